@@ -1,0 +1,243 @@
+/*
+ * CPU oracle for batch-1 greedy decode of a dense Llama-style decoder. TEST INFRASTRUCTURE ONLY:
+ * it is loaded by the tests, by __graft_entry__.smoke() and by the bench's CPU-baseline leg, never by
+ * the product path, and it shares no code, header, table or constant with the GPU library.
+ *
+ * What it computes (the Kog monokernel pages, "inside the monokernel" and the fusion list in the same
+ * section: the monokernel folds RMSNorm, repacks QKV, precomputes RoPE and recomputes attention; all four
+ * are exact reformulations of the plain forward, so this file computes the plain forward, unfolded):
+ *   x = E[t]; per layer: u = rmsnorm(x) * g_attn; q, k, v = Wq u, Wk u, Wv u; RoPE(q, k, pos);
+ *   cache[pos] = fp16(k), fp16(v); o_h = softmax(q_h K_g^T / sqrt(dh)) V_g with g = h / (Hq / Hkv);
+ *   x += Wo o; u = rmsnorm(x) * g_ffn; x += Wd (silu(Wg u) * (Wu u));
+ *   logits = Wlm (rmsnorm(x) * g_final); next token = argmax (lowest index on ties).
+ * The pages leave the architecture details open (pre-norm, no biases, SwiGLU, rotate-half RoPE, 0-based
+ * positions, contiguous GQA groups, fp16 only in weights and K/V cache); this file takes that plainest
+ * Llama reading.
+ *
+ * Precision: fp16 weights and K/V cache, arithmetic in REAL = float (orc_*_f32) or double (orc_*_f64).
+ * Build with -ffp-contract=off so that every product and sum is rounded as written.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, max_seq;
+  float rope_theta, rms_eps;
+} orc_config;
+
+typedef struct {
+  const uint16_t *embed, *lm_head, *final_norm;
+  const uint16_t *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+  const uint16_t *const *ffn_norm, *const *w_gate, *const *w_up, *const *w_down;
+} orc_weights;
+
+typedef struct {
+  orc_config cfg;
+  orc_weights w; /* borrowed: the caller keeps every tensor alive */
+  const uint16_t **ptrs; /* owned copies of the per-layer pointer arrays */
+  int precision;         /* 32 or 64 */
+  int pos;
+  uint16_t *kv; /* [L][2][Hkv][max_seq][dh] fp16 bits */
+  void *x, *u, *q, *k, *v, *o, *t, *g, *up, *scores;
+} orc_model;
+
+/* ---- binary16 <-> real, from the format's definition ---------------------------------------------- */
+
+static float half_table[65536];
+static int half_table_ready = 0;
+
+static double half_decode(uint16_t h) {
+  int sign = h >> 15, e = (h >> 10) & 31, f = h & 1023;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -24); /* subnormal: f * 2^-24 */
+  else if (e == 31)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp((double)(1024 + f), e - 25); /* (1 + f/1024) * 2^(e-15) */
+  return sign ? -v : v;
+}
+
+static void half_init(void) {
+  if (half_table_ready) return;
+  for (int i = 0; i < 65536; ++i) half_table[i] = (float)half_decode((uint16_t)i);
+  half_table_ready = 1;
+}
+
+static inline float half_value(uint16_t h) { return half_table[h]; }
+
+/* Round a real to the nearest binary16 (ties to even) by scaling to the format's quantum at that
+ * magnitude and rounding to an integer there (nearbyint in the default round-to-nearest-even mode). */
+static uint16_t half_bits(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (isnan(v)) return 0x7E00;
+  if (a == 0.0) return sign;
+  int E;
+  frexp(a, &E); /* a = m * 2^E, m in [0.5, 1): leading bit weighs 2^(E-1) */
+  int lead = E - 1;
+  double quantum = ldexp(1.0, (lead < -14 ? -14 : lead) - 10);
+  double r = nearbyint(a / quantum) * quantum; /* exact: scaling by powers of two */
+  if (r >= 65520.0) return sign | 0x7C00;
+  if (r < ldexp(1.0, -14)) return sign | (uint16_t)(r / ldexp(1.0, -24)); /* subnormal (or min normal) */
+  frexp(r, &E);
+  lead = E - 1;
+  uint16_t mant = (uint16_t)(r / ldexp(1.0, lead - 10) - 1024.0);
+  return sign | (uint16_t)((lead + 15) << 10) | mant;
+}
+
+/* ---- the two instantiations ----------------------------------------------------------------------- */
+
+#define REAL float
+#define NAME(x) x##_f32
+#define SQRT sqrtf
+#define EXP expf
+#include "oracle_impl.h"
+#undef REAL
+#undef NAME
+#undef SQRT
+#undef EXP
+
+#define REAL double
+#define NAME(x) x##_f64
+#define SQRT sqrt
+#define EXP exp
+#include "oracle_impl.h"
+#undef REAL
+#undef NAME
+#undef SQRT
+#undef EXP
+
+/* ---- exported API (ctypes) ------------------------------------------------------------------------ */
+
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int orc_get_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+double orc_half_to_double(uint16_t h) { return half_decode(h); }
+uint16_t orc_double_to_half(double v) { return half_bits(v); }
+
+int orc_argmax_f32(const float *v, int n) {
+  int best = 0;
+  for (int i = 1; i < n; ++i)
+    if (v[i] > v[best]) best = i;
+  return best;
+}
+
+int orc_argmax_f64(const double *v, int n) {
+  int best = 0;
+  for (int i = 1; i < n; ++i)
+    if (v[i] > v[best]) best = i;
+  return best;
+}
+
+void orc_rmsnorm_f32(const float *x, const uint16_t *g, int n, float eps, float *out) { half_init(); rmsnorm_f32(x, g, n, eps, out); }
+void orc_rmsnorm_f64(const double *x, const uint16_t *g, int n, double eps, double *out) { half_init(); rmsnorm_f64(x, g, n, eps, out); }
+void orc_gemv_f32(const uint16_t *W, const float *x, int M, int K, float *y) { half_init(); gemv_f32(W, x, M, K, y); }
+void orc_gemv_f64(const uint16_t *W, const double *x, int M, int K, double *y) { half_init(); gemv_f64(W, x, M, K, y); }
+void orc_rope_f32(float *v, int dh, int pos, double theta) { rope_f32(v, dh, pos, theta); }
+void orc_rope_f64(double *v, int dh, int pos, double theta) { rope_f64(v, dh, pos, theta); }
+float orc_silu_f32(float z) { return silu_f32(z); }
+double orc_silu_f64(double z) { return silu_f64(z); }
+
+void orc_attention_f32(const float *q, const uint16_t *K, const uint16_t *V, int c, int dh, float *out) {
+  half_init();
+  float *sc = (float *)malloc(sizeof(float) * (size_t)(c > 0 ? c : 1));
+  attention_f32(q, K, V, c, dh, (size_t)dh, sc, out);
+  free(sc);
+}
+
+void orc_attention_f64(const double *q, const uint16_t *K, const uint16_t *V, int c, int dh, double *out) {
+  half_init();
+  double *sc = (double *)malloc(sizeof(double) * (size_t)(c > 0 ? c : 1));
+  attention_f64(q, K, V, c, dh, (size_t)dh, sc, out);
+  free(sc);
+}
+
+orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision) {
+  half_init();
+  if (!cfg || !w || (precision != 32 && precision != 64)) return NULL;
+  if (cfg->n_layers < 0 || cfg->d_model <= 0 || cfg->n_heads <= 0 || cfg->n_kv_heads <= 0 ||
+      cfg->n_heads % cfg->n_kv_heads || cfg->head_dim <= 0 || cfg->head_dim % 2 || cfg->ffn_dim <= 0 ||
+      cfg->vocab <= 0 || cfg->max_seq <= 0)
+    return NULL;
+  orc_model *m = (orc_model *)calloc(1, sizeof(orc_model));
+  m->cfg = *cfg;
+  m->precision = precision;
+  int L = cfg->n_layers;
+  m->ptrs = (const uint16_t **)calloc((size_t)(9 * (L > 0 ? L : 1)), sizeof(uint16_t *));
+  const uint16_t *const *src[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
+  const uint16_t *const **dst[9] = {&m->w.attn_norm, &m->w.wq, &m->w.wk, &m->w.wv, &m->w.wo,
+                                    &m->w.ffn_norm, &m->w.w_gate, &m->w.w_up, &m->w.w_down};
+  for (int j = 0; j < 9; ++j) {
+    const uint16_t **slot = m->ptrs + (size_t)j * (L > 0 ? L : 1);
+    for (int l = 0; l < L; ++l) slot[l] = src[j][l];
+    *dst[j] = slot;
+  }
+  m->w.embed = w->embed;
+  m->w.lm_head = w->lm_head;
+  m->w.final_norm = w->final_norm;
+  size_t es = precision == 32 ? sizeof(float) : sizeof(double);
+  int d = cfg->d_model, qd = cfg->n_heads * cfg->head_dim, kd = cfg->n_kv_heads * cfg->head_dim;
+  int wide = d > qd ? d : qd;
+  m->kv = (uint16_t *)calloc((size_t)L * 2 * cfg->n_kv_heads * cfg->max_seq * cfg->head_dim + 1, 2);
+  m->x = calloc((size_t)d, es);
+  m->u = calloc((size_t)d, es);
+  m->q = calloc((size_t)qd, es);
+  m->k = calloc((size_t)kd, es);
+  m->v = calloc((size_t)kd, es);
+  m->o = calloc((size_t)qd, es);
+  m->t = calloc((size_t)wide, es);
+  m->g = calloc((size_t)cfg->ffn_dim, es);
+  m->up = calloc((size_t)cfg->ffn_dim, es);
+  m->scores = calloc((size_t)cfg->max_seq, es);
+  return m;
+}
+
+void orc_destroy(orc_model *m) {
+  if (!m) return;
+  free(m->ptrs);
+  free(m->kv);
+  free(m->x); free(m->u); free(m->q); free(m->k); free(m->v);
+  free(m->o); free(m->t); free(m->g); free(m->up); free(m->scores);
+  free(m);
+}
+
+int orc_pos(const orc_model *m) { return m->pos; }
+void orc_reset(orc_model *m) { m->pos = 0; }
+
+/* Forward one token; logits is float[vocab] (precision 32) or double[vocab] (precision 64).
+ * Returns 0, or -1 when the cache is full or the token is out of range. */
+int orc_forward(orc_model *m, int token, void *logits) {
+  if (m->pos >= m->cfg.max_seq || token < 0 || token >= m->cfg.vocab) return -1;
+  if (m->precision == 32)
+    forward_f32(m, token, (float *)logits);
+  else
+    forward_f64(m, token, (double *)logits);
+  return 0;
+}
+
+/* Read back the cached K (kv = 0) or V (kv = 1) row of (layer, kv_head, pos) as fp16 bits. */
+void orc_kv_row(const orc_model *m, int layer, int kv, int head, int pos, uint16_t *out) {
+  const orc_config *c = &m->cfg;
+  size_t S = (size_t)c->max_seq * c->head_dim;
+  const uint16_t *p = m->kv + ((size_t)layer * 2 + kv) * c->n_kv_heads * S + head * S + (size_t)pos * c->head_dim;
+  memcpy(out, p, sizeof(uint16_t) * (size_t)c->head_dim);
+}

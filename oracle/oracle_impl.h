@@ -1,0 +1,114 @@
+/*
+ * Body of the CPU oracle, compiled twice by oracle.c: once with REAL = float (the reference precision:
+ * fp16 weights and KV cache, fp32 arithmetic) and once with REAL = double (to bound the fp32 version's
+ * own rounding). Every loop is the plain definition, summed in index order.
+ *
+ * Expects from the includer: REAL, NAME(x), SQRT(x), EXP(x).
+ */
+
+/* u = x / sqrt(mean(x^2) + eps) * g  (RMSNorm; the gain g is fp16). */
+static void NAME(rmsnorm)(const REAL *x, const uint16_t *g, int n, REAL eps, REAL *out) {
+  REAL ss = 0;
+  for (int i = 0; i < n; ++i) ss += x[i] * x[i];
+  REAL denom = SQRT(ss / (REAL)n + eps);
+  for (int i = 0; i < n; ++i) out[i] = (x[i] / denom) * (REAL)half_value(g[i]);
+}
+
+/* y = W x with W [M, K] row-major fp16, each row summed sequentially over k. */
+static void NAME(gemv)(const uint16_t *W, const REAL *x, int M, int K, REAL *y) {
+#pragma omp parallel for schedule(static) if (M >= 256)
+  for (int r = 0; r < M; ++r) {
+    const uint16_t *w = W + (size_t)r * K;
+    REAL acc = 0;
+    for (int k = 0; k < K; ++k) acc += (REAL)half_value(w[k]) * x[k];
+    y[r] = acc;
+  }
+}
+
+/* Rotary embedding, "rotate-half" pairing: dimension i is paired with i + dh/2 (i < dh/2), rotated by
+ * the angle pos * theta^(-2i/dh). The angle and its cosine and sine are evaluated in fp64. */
+static void NAME(rope)(REAL *v, int dh, int pos, double theta) {
+  int half = dh / 2;
+  for (int i = 0; i < half; ++i) {
+    double angle = (double)pos * pow(theta, -2.0 * (double)i / (double)dh);
+    REAL c = (REAL)cos(angle), s = (REAL)sin(angle);
+    REAL a = v[i], b = v[i + half];
+    v[i] = a * c - b * s;
+    v[i + half] = b * c + a * s;
+  }
+}
+
+/* One attention head over c cached positions: s_j = q . K[j] / sqrt(dh); p = softmax(s) with the maximum
+ * subtracted; out = sum_j p_j V[j]. K and V are fp16 rows of length dh, `stride` elements apart. */
+static void NAME(attention)(const REAL *q, const uint16_t *K, const uint16_t *V, int c, int dh, size_t stride,
+                            REAL *scores, REAL *out) {
+  REAL root = SQRT((REAL)dh);
+  for (int j = 0; j < c; ++j) {
+    const uint16_t *k = K + (size_t)j * stride;
+    REAL dot = 0;
+    for (int e = 0; e < dh; ++e) dot += q[e] * (REAL)half_value(k[e]);
+    scores[j] = dot / root;
+  }
+  REAL m = scores[0];
+  for (int j = 1; j < c; ++j)
+    if (scores[j] > m) m = scores[j];
+  REAL l = 0;
+  for (int j = 0; j < c; ++j) {
+    scores[j] = EXP(scores[j] - m);
+    l += scores[j];
+  }
+  for (int e = 0; e < dh; ++e) out[e] = 0;
+  for (int j = 0; j < c; ++j) {
+    REAL p = scores[j] / l;
+    const uint16_t *v = V + (size_t)j * stride;
+    for (int e = 0; e < dh; ++e) out[e] += p * (REAL)half_value(v[e]);
+  }
+}
+
+/* silu(z) = z / (1 + exp(-z)). */
+static REAL NAME(silu)(REAL z) { return z / ((REAL)1 + EXP(-z)); }
+
+/* One decoder forward of `token` at position m->pos: appends K and V (rounded to fp16) to the cache,
+ * writes the logits of the next position, advances pos. */
+static void NAME(forward)(orc_model *m, int token, REAL *logits) {
+  const orc_config *c = &m->cfg;
+  const int d = c->d_model, Hq = c->n_heads, Hkv = c->n_kv_heads, dh = c->head_dim, F = c->ffn_dim;
+  const int group = Hq / Hkv, pos = m->pos;
+  const size_t S = (size_t)c->max_seq * dh; /* elements per [layer][k|v][kv-head] plane */
+  REAL *x = (REAL *)m->x, *u = (REAL *)m->u, *q = (REAL *)m->q, *k = (REAL *)m->k, *v = (REAL *)m->v;
+  REAL *o = (REAL *)m->o, *t = (REAL *)m->t, *g = (REAL *)m->g, *up = (REAL *)m->up, *sc = (REAL *)m->scores;
+
+  for (int i = 0; i < d; ++i) x[i] = (REAL)half_value(m->w.embed[(size_t)token * d + i]);
+
+  for (int l = 0; l < c->n_layers; ++l) {
+    NAME(rmsnorm)(x, m->w.attn_norm[l], d, (REAL)c->rms_eps, u);
+    NAME(gemv)(m->w.wq[l], u, Hq * dh, d, q);
+    NAME(gemv)(m->w.wk[l], u, Hkv * dh, d, k);
+    NAME(gemv)(m->w.wv[l], u, Hkv * dh, d, v);
+    for (int h = 0; h < Hq; ++h) NAME(rope)(q + h * dh, dh, pos, c->rope_theta);
+    for (int h = 0; h < Hkv; ++h) NAME(rope)(k + h * dh, dh, pos, c->rope_theta);
+
+    uint16_t *Kl = m->kv + (size_t)l * 2 * Hkv * S, *Vl = Kl + (size_t)Hkv * S;
+    for (int h = 0; h < Hkv; ++h)
+      for (int e = 0; e < dh; ++e) {
+        Kl[h * S + (size_t)pos * dh + e] = half_bits((double)k[h * dh + e]);
+        Vl[h * S + (size_t)pos * dh + e] = half_bits((double)v[h * dh + e]);
+      }
+    for (int h = 0; h < Hq; ++h) {
+      int kvh = h / group;
+      NAME(attention)(q + h * dh, Kl + kvh * S, Vl + kvh * S, pos + 1, dh, (size_t)dh, sc, o + h * dh);
+    }
+    NAME(gemv)(m->w.wo[l], o, d, Hq * dh, t);
+    for (int i = 0; i < d; ++i) x[i] += t[i];
+
+    NAME(rmsnorm)(x, m->w.ffn_norm[l], d, (REAL)c->rms_eps, u);
+    NAME(gemv)(m->w.w_gate[l], u, F, d, g);
+    NAME(gemv)(m->w.w_up[l], u, F, d, up);
+    for (int i = 0; i < F; ++i) g[i] = NAME(silu)(g[i]) * up[i];
+    NAME(gemv)(m->w.w_down[l], g, d, F, t);
+    for (int i = 0; i < d; ++i) x[i] += t[i];
+  }
+  NAME(rmsnorm)(x, m->w.final_norm, d, (REAL)c->rms_eps, u);
+  NAME(gemv)(m->w.lm_head, u, c->vocab, d, logits);
+  m->pos = pos + 1;
+}
