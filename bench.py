@@ -1,0 +1,278 @@
+"""Batch-1 greedy decode throughput of the 2B fp16 Llama-style workload on GB300, as one JSON line.
+
+A step is one kie_decode of 1,024 tokens after a 128-token prompt (prefill untimed for `value`): one launch
+of the persistent monokernel. `value` = decode tokens / device time (CUDA events on the library's stream);
+`e2e` = the same tokens through the public host-buffer API (reset + prefill from a host prompt + decode
+into a host array, wall clock), so it includes the prompt and both copies. Weights (3.9 GB) are larger than
+L2 and every token streams them all, so no L2 flush is needed between steps.
+
+--impl reference times the CPU oracle (oracle/, plain C) on the host cores on a bounded sample of the same
+workload. With N > 1 (torchrun) every rank runs an independent replica: the path has no data exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tok/s, 2B fp16 on 1 GB300; MBU vs HBM peak"
+WORKLOAD = "llama2b_p128_n1024"
+PROMPT, NEW = 128, 1024
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def algorithmic_bytes(model, prompt_len, n):
+    """Bytes one decode of n tokens must move: every weight once per token, plus the K/V prefix it attends
+    over (the token at position p attends over p + 1 positions)."""
+    w = model.weight_bytes_per_token() * n
+    kv = sum(model.kv_bytes_per_token(prompt_len + t + 1) for t in range(n))
+    return w + kv
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc = index, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle, timed on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+    from synth.configs import TWO_B
+
+    per_step = 2  # decode forwards per step: a bounded sample (~1-3 s of CPU time each on 16 cores)
+    w = synth.model_weights(TWO_B)
+    prompt = synth.tokens(TWO_B.seed, PROMPT, TWO_B.vocab)
+    m = oracle.Model(TWO_B, w, PROMPT + (args.warmup + args.steps) * per_step + 1, 32)
+    ctx_prompt = prompt[:8]  # short untimed prefill: the sample measures decode forwards only
+    cur = m.prefill(ctx_prompt)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for _ in range(per_step):
+            cur = m.forward(oracle.argmax(cur))
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = args.steps * per_step / total
+    cores = oracle.threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": f"{per_step} greedy decode forwards per step after an "
+                   f"8-token prefill (2B model, full weights)", "weights": "fp16", "kv_cache": "fp16"},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} x {per_step} decode forwards of the 2B model"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_sample(seconds_budget=20.0):
+    """The oracle as it stands on the host cores: greedy decode forwards of the 2B model (bounded)."""
+    import oracle
+    import synth
+    from synth.configs import TWO_B
+
+    w = synth.model_weights(TWO_B)
+    prompt = synth.tokens(TWO_B.seed, 8, TWO_B.vocab)
+    m = oracle.Model(TWO_B, w, 64, 32)
+    cur = m.prefill(prompt)
+    n, t0 = 0, time.perf_counter()
+    while n < 40:
+        cur = m.forward(oracle.argmax(cur))
+        n += 1
+        if time.perf_counter() - t0 > seconds_budget:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} greedy decode forwards of the 2B model after an 8-token prefill ({dt:.1f} s)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kie", choices=["kie", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    import persistent_monokernel_decode_gb300 as kie
+    import synth
+    from synth.configs import TWO_B
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    kie.build()
+
+    w = synth.model_weights(TWO_B)
+    prompt = synth.tokens(TWO_B.seed, PROMPT, TWO_B.vocab)
+    dec = kie.Decoder(TWO_B, w, max_seq=PROMPT + NEW)
+    del w
+    out = torch.empty(NEW, dtype=torch.int32, device="cuda")
+    stream = dec.stream
+
+    def prefill():
+        dec.reset()
+        dec.prefill(prompt)
+
+    for _ in range(args.warmup):
+        prefill()
+        dec.decode_async(NEW, out)
+        dec.sync()
+
+    clocks = ClockSampler(local)
+    times = []
+    stats = None
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for _ in range(args.steps):
+        prefill()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dec.decode_async(NEW, out)
+        e1.record(stream)
+        dec.sync()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    stats = dec.barrier_stats()
+    step_s = sum(times) / len(times)
+    if pg:
+        t = torch.tensor([step_s], device="cuda", dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        step_s = float(t.item())
+    value = world * NEW / step_s
+
+    # end to end through the host-buffer API: reset + prefill(host prompt) + decode(n, host tokens)
+    e2e_times = []
+    host_out = np.empty(NEW, dtype=np.int32)
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dec.reset()
+        dec.prefill(prompt)
+        host_out[:] = dec.decode(NEW)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            e2e_times.append(dt)
+    e2e_step = sum(e2e_times) / len(e2e_times)
+    if pg:
+        t = torch.tensor([e2e_step], device="cuda", dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_step = float(t.item())
+
+    peaks, peak_kind = measured_peaks()
+    bytes_launch = algorithmic_bytes(TWO_B, PROMPT, NEW)
+    achieved = bytes_launch / step_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "prompt": PROMPT, "decode_tokens": NEW, "weights": "fp16",
+                   "kv_cache": "fp16", "l2": "no flush: 3.9 GB of weights (> 129 MB L2) streamed per token",
+                   "parallelism": "replicas" if world > 1 else "single GPU", "n_cta": dec.n_cta},
+        "e2e": {"value": world * NEW / e2e_step, "unit": "tok/s", "h2d_bytes_per_step": PROMPT * 4,
+                "d2h_bytes_per_step": NEW * 4 + 8,
+                "timed": "reset + prefill(128-token host prompt) + decode(1024 -> host array), wall clock"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "peak_kind": f"{peak_kind} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": bytes_launch},
+        "mbu": {"measured_peak": achieved / peaks["hbm_gbs"], "spec_8tbs": achieved / 8000.0},
+        "barriers": {"per_token": stats["barriers"] / NEW, "mean_latency_ns": stats["mean_latency_ns"],
+                     "mean_wait_ns": stats["mean_wait_ns"],
+                     "wait_us_per_token": stats["mean_wait_ns"] * stats["barriers"] / NEW / 1e3},
+        "clocks": clk,
+    }
+    dec.close()
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * kie.h -- C ABI of the GB300 (sm_103a) persistent decode monokernel.
+ *
+ * The library runs batch-1 greedy decode of a dense Llama-style decoder (fp16 weights and KV cache, fp32
+ * arithmetic) as ONE persistent cooperative kernel per call, one CTA per SM, that loops over all requested
+ * tokens and all layers without returning to the host. This is the "monokernel" of the Kog Inference
+ * Engine pages ("Inside the monokernel: a single resident GPU program that never returns control"): the
+ * host launches once, the device embeds, projects, attends, samples and feeds the next token back itself.
+ *
+ * Conventions for every entry point:
+ *   - Return value: KIE_OK (0) or a negative KIE_ERR_* code. kie_last_error() gives a message.
+ *   - Weights are IEEE binary16 bit patterns (uint16_t), row-major [out_features, in_features].
+ *   - Pointers are HOST pointers unless the name or comment says "_dev" / "device".
+ *   - A kie_ctx is not thread-safe: calls on one ctx must be serialised by the caller. All GPU work of a
+ *     ctx is issued on the stream given at creation (NULL = the legacy default stream).
+ *   - Positions are 0-based; the first prompt token is at position 0.
+ */
+#ifndef KIE_H
+#define KIE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  KIE_OK = 0,
+  KIE_ERR_INVALID = -1,  /* bad argument, unsupported dimension, or call out of order */
+  KIE_ERR_OOM = -2,      /* a device allocation failed */
+  KIE_ERR_CAPACITY = -3, /* position + n would exceed max_seq */
+  KIE_ERR_CUDA = -4,     /* a CUDA runtime call failed (message in kie_last_error) */
+  KIE_ERR_LAUNCH = -5,   /* the cooperative grid (one CTA per SM) could not be made co-resident */
+  KIE_ERR_TIMEOUT = -6   /* a device-side wait gave up; the kernel exited cleanly, the ctx is reset */
+};
+
+/* Model shape. Supported: head_dim in {64, 128}; n_heads % n_kv_heads == 0; d_model, ffn_dim and
+ * n_heads*head_dim multiples of 8; n_layers >= 1; vocab >= 2. rope_theta is the RoPE base, rms_eps the
+ * RMSNorm epsilon. */
+typedef struct {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, max_seq;
+  float rope_theta, rms_eps;
+} kie_config;
+
+/* Host weights (fp16 bits). Per-layer fields are arrays of n_layers host pointers. Shapes:
+ * embed, lm_head [vocab, d_model]; final_norm, attn_norm[l], ffn_norm[l] [d_model];
+ * wq [n_heads*head_dim, d_model]; wk, wv [n_kv_heads*head_dim, d_model]; wo [d_model, n_heads*head_dim];
+ * w_gate, w_up [ffn_dim, d_model]; w_down [d_model, ffn_dim].
+ * Ownership: read during kie_create only; the caller may free them afterwards. */
+typedef struct {
+  const uint16_t *embed, *lm_head, *final_norm;
+  const uint16_t *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+  const uint16_t *const *ffn_norm, *const *w_gate, *const *w_up, *const *w_down;
+} kie_weights;
+
+typedef struct kie_ctx kie_ctx;
+
+/* Device buffer sizes a ctx needs (bytes), for callers that allocate device memory themselves. */
+typedef struct {
+  size_t weights_bytes;   /* repacked weights + embedding table */
+  size_t kv_bytes;        /* K/V cache [n_layers][2][n_kv_heads][max_seq][head_dim] fp16 */
+  size_t workspace_bytes; /* activations, split-attention partials, RoPE table, logits, control words */
+  int n_cta;              /* CTAs of the persistent grid the layout was planned for */
+} kie_buffer_sizes;
+
+/* Sizes for `cfg` on the current device (n_cta = its SM count when the argument is 0).
+ * Errors: KIE_ERR_INVALID for an unsupported cfg; KIE_ERR_CUDA if the device cannot be queried. */
+int kie_query_buffers(const kie_config *cfg, int n_cta, kie_buffer_sizes *out);
+
+/* Create a ctx: validates cfg, repacks the weights (QKV fused with RoPE pairs made adjacent, gate/up
+ * interleaved, RMSNorm gains folded into the next matrix, rows tiled per CTA -- the fusion list of the
+ * "inside the monokernel" section of the monokernel pages), uploads them, builds the RoPE table and
+ * zeroes the KV cache. `stream` is a cudaStream_t or NULL. The ctx allocates its own device memory
+ * (cudaMalloc) and frees it in kie_destroy. On error *out is NULL. */
+int kie_create(const kie_config *cfg, const kie_weights *w, void *stream, kie_ctx **out);
+
+/* As kie_create, but the device memory is provided by the caller (e.g. allocated with PyTorch) and stays
+ * owned by the caller: it must outlive the ctx. Each buffer must be 256-byte aligned and at least the size
+ * kie_query_buffers returned (for n_cta = 0). kie_create_with_buffers still allocates one temporary
+ * staging buffer of the largest repacked matrix while it runs, and frees it before returning. */
+int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *stream, void *weights_dev,
+                            size_t weights_bytes, void *kv_dev, size_t kv_bytes, void *workspace_dev,
+                            size_t workspace_bytes, kie_ctx **out);
+
+/* Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 in one
+ * launch of the monokernel in forced-token mode; keeps the logits of the last one (so the next decode can
+ * start). Synchronous. Errors: INVALID (n < 1, bad id), CAPACITY, CUDA, LAUNCH, TIMEOUT. */
+int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n);
+
+/* Greedy decode of n tokens in ONE launch (the hot path). Token i is the argmax of the current logits
+ * (lowest id on ties); the kernel then runs the forward of that token at the next position, whose logits
+ * are the current ones for token i+1. So n tokens cost n forwards, and decode(a) then decode(b) gives the
+ * same tokens as decode(a+b). Requires a prior prefill (INVALID otherwise). `out_tokens` is a host array of
+ * n int32; the call synchronises the stream. Errors: INVALID, CAPACITY, CUDA, LAUNCH, TIMEOUT. */
+int kie_decode(kie_ctx *ctx, int n, int32_t *out_tokens);
+
+/* As kie_decode, but writes the n tokens to DEVICE memory `out_tokens_dev` and returns right after the
+ * launch is enqueued on the ctx stream (no synchronisation). Device-side errors are reported by the next
+ * kie_sync(). */
+int kie_decode_async(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
+
+/* Wait for the ctx stream and report the status word of the last launch (KIE_OK or KIE_ERR_TIMEOUT). */
+int kie_sync(kie_ctx *ctx);
+
+/* Teacher forcing, for tests: for i in [0, n): out_tokens[i] = argmax of the current logits (what greedy
+ * decode would emit), then the forward consumes forced[i] (not the argmax) at the next position; if
+ * out_logits is not NULL it receives the logits of that forward ([n, vocab] fp32, host). Synchronous.
+ * Requires a prior prefill. */
+int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_tokens, float *out_logits);
+
+/* Copy the current logits (those the next emitted token is the argmax of) to host float[vocab]. */
+int kie_get_logits(kie_ctx *ctx, float *out);
+
+/* Number of tokens in the KV cache (the position the next forward writes). */
+int kie_position(const kie_ctx *ctx);
+
+/* Forget the sequence: position 0, no current logits. The KV cache is not cleared (it is overwritten). */
+int kie_reset(kie_ctx *ctx);
+
+/* Device-side wait limit in nanoseconds for grid barriers and ring waits (default 1e9). */
+int kie_set_timeout_ns(kie_ctx *ctx, uint64_t ns);
+
+/* Barrier timing of the last launch, from %globaltimer stamps taken by every CTA:
+ * barriers = grid barriers the launch passed; mean_wait_ns = mean over CTAs and barriers of the time a CTA
+ * spent waiting in a barrier (idle time); mean_latency_ns = mean over barriers of the SHORTEST wait among
+ * CTAs (the last CTA to arrive waits only for the barrier's own latency); total_ns = launch duration seen
+ * by CTA 0. */
+typedef struct {
+  int64_t barriers;
+  double mean_wait_ns, mean_latency_ns, total_ns;
+} kie_barrier_stats;
+int kie_get_barrier_stats(kie_ctx *ctx, kie_barrier_stats *out);
+
+/* Test hook (fault injection on the host side of the contract): if cta >= 0, that CTA skips its arrival
+ * at grid barrier number `barrier` of the next launch, so every other CTA's wait runs out and the launch
+ * returns KIE_ERR_TIMEOUT after the configured limit. No GPU fault, trap or unbounded wait is involved. */
+int kie_debug_skip_arrival(kie_ctx *ctx, int cta, int barrier);
+
+int kie_n_cta(const kie_ctx *ctx);
+const char *kie_last_error(const kie_ctx *ctx); /* ctx may be NULL: last error of a failed create */
+void kie_destroy(kie_ctx *ctx);
+
+/* ---- standalone GEMV (the same device code as the monokernel's projections) -------------------------
+ * y[M] (fp32) = W[M, K] (fp16) . x[K] (fp16), fp32 accumulation, weights streamed through the same
+ * shared-memory ring. W must first be packed into the per-CTA tile layout (kie_gemv_pack), as the
+ * decoder's weights are at creation. Requirements: M even, K a multiple of 8, M, K >= 2. */
+
+/* Bytes of the packed matrix (= 2*M*K). */
+size_t kie_gemv_packed_bytes(int M, int K);
+
+/* Pack row-major W_dev [M, K] into packed_dev for an n_cta-CTA grid (0 = SM count), on `stream`.
+ * Both are device pointers, 16-byte aligned, not overlapping. Asynchronous. */
+int kie_gemv_pack(const uint16_t *W_dev, int M, int K, int n_cta, uint16_t *packed_dev, void *stream);
+
+/* y_dev = W . x_dev with W packed for the same n_cta. One launch of n_cta CTAs on `stream`; asynchronous. */
+int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, int M, int K, int n_cta,
+             void *stream);
+
+/* Host-side layout query (no GPU needed): element offset of W[r][c] inside the packed matrix. */
+int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c);
+
+/* Host-side layout query: first and one-past-last row owned by CTA `cta` (pairs of rows are never split). */
+int kie_rows_of_cta(int M, int n_cta, int cta, int *r0, int *r1);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIE_H */

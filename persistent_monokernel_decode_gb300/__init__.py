@@ -1,0 +1,306 @@
+"""Python binding of the GB300 persistent decode monokernel (C ABI in include/kie.h).
+
+The binding only marshals arguments: every step of decode runs in the CUDA kernels of ``libkie.so``.
+PyTorch is used for two things only, device memory (``torch.empty`` buffers handed to
+``kie_create_with_buffers``) and the CUDA stream the library launches on. There is no CPU fallback: if
+the extension is not built, or no GPU is present, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(_ROOT, "include")
+_BUILD = os.path.join(_ROOT, "_build")
+LIB_PATH = os.path.join(_HERE, "libkie.so")
+SOURCES = ("kie_api.cu", "kie_decode.cu", "kie_gemv.cu")
+HEADERS = ("kie_layout.h", "kie_device.cuh", "kie_decode.cuh")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+KIE_OK, KIE_ERR_INVALID, KIE_ERR_OOM, KIE_ERR_CAPACITY = 0, -1, -2, -3
+KIE_ERR_CUDA, KIE_ERR_LAUNCH, KIE_ERR_TIMEOUT = -4, -5, -6
+ERROR_NAMES = {0: "KIE_OK", -1: "KIE_ERR_INVALID", -2: "KIE_ERR_OOM", -3: "KIE_ERR_CAPACITY", -4: "KIE_ERR_CUDA",
+               -5: "KIE_ERR_LAUNCH", -6: "KIE_ERR_TIMEOUT"}
+
+
+# ---- build ------------------------------------------------------------------------------------------
+
+def _nvcc() -> str:
+    if os.environ.get("NVCC"):
+        return os.environ["NVCC"]
+    return "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc"
+
+
+def compile_cmds() -> list[list[str]]:
+    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", f"-I{_INCLUDE}", f"-I{_CSRC}"]
+    return [[_nvcc(), *flags, "-c", os.path.join(_CSRC, s), "-o", os.path.join(_BUILD, s + ".o")] for s in SOURCES]
+
+
+def link_cmd() -> list[str]:
+    return [_nvcc(), *ARCH, "-shared", "-o", LIB_PATH, *[os.path.join(_BUILD, s + ".o") for s in SOURCES]]
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(_CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(_INCLUDE, "kie.h")]
+    return any(os.path.getmtime(f) > t for f in deps)
+
+
+def build(force: bool = False) -> str:
+    """Compile libkie.so in-tree for sm_103a (three translation units in parallel, then link)."""
+    if not force and not _stale():
+        return LIB_PATH
+    os.makedirs(_BUILD, exist_ok=True)
+    with ThreadPoolExecutor(len(SOURCES)) as ex:
+        results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), compile_cmds()))
+    for r in results:
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + r.stdout + r.stderr)
+    r = subprocess.run(link_cmd(), capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc link failed:\n" + r.stdout + r.stderr)
+    return LIB_PATH
+
+
+# ---- C structs --------------------------------------------------------------------------------------
+
+P = ctypes.c_void_p
+
+
+class KieConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("n_layers", "d_model", "n_heads", "n_kv_heads", "head_dim",
+                                             "ffn_dim", "vocab", "max_seq")] + \
+               [("rope_theta", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+class KieWeights(ctypes.Structure):
+    _fields_ = [(n, P) for n in ("embed", "lm_head", "final_norm", "attn_norm", "wq", "wk", "wv", "wo",
+                                 "ffn_norm", "w_gate", "w_up", "w_down")]
+
+
+class KieBufferSizes(ctypes.Structure):
+    _fields_ = [("weights_bytes", ctypes.c_size_t), ("kv_bytes", ctypes.c_size_t),
+                ("workspace_bytes", ctypes.c_size_t), ("n_cta", ctypes.c_int)]
+
+
+class KieBarrierStats(ctypes.Structure):
+    _fields_ = [("barriers", ctypes.c_int64), ("mean_wait_ns", ctypes.c_double),
+                ("mean_latency_ns", ctypes.c_double), ("total_ns", ctypes.c_double)]
+
+
+# Every entry point of include/kie.h with its ctypes signature.
+SIGNATURES = {
+    "kie_query_buffers": ([P, ctypes.c_int, P], ctypes.c_int),
+    "kie_create": ([P, P, P, P], ctypes.c_int),
+    "kie_create_with_buffers": ([P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P, ctypes.c_size_t, P], ctypes.c_int),
+    "kie_prefill": ([P, P, ctypes.c_int], ctypes.c_int),
+    "kie_decode": ([P, ctypes.c_int, P], ctypes.c_int),
+    "kie_decode_async": ([P, ctypes.c_int, P], ctypes.c_int),
+    "kie_sync": ([P], ctypes.c_int),
+    "kie_decode_forced": ([P, ctypes.c_int, P, P, P], ctypes.c_int),
+    "kie_get_logits": ([P, P], ctypes.c_int),
+    "kie_position": ([P], ctypes.c_int),
+    "kie_reset": ([P], ctypes.c_int),
+    "kie_set_timeout_ns": ([P, ctypes.c_uint64], ctypes.c_int),
+    "kie_get_barrier_stats": ([P, P], ctypes.c_int),
+    "kie_debug_skip_arrival": ([P, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+    "kie_n_cta": ([P], ctypes.c_int),
+    "kie_last_error": ([P], ctypes.c_char_p),
+    "kie_destroy": ([P], None),
+    "kie_gemv_packed_bytes": ([ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
+    "kie_gemv_pack": ([P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
+    "kie_gemv": ([P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P], ctypes.c_int),
+    "kie_packed_offset": ([ctypes.c_int] * 5, ctypes.c_int64),
+    "kie_rows_of_cta": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libkie.so. Raises if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: run __graft_entry__.build() (or "
+                               "persistent_monokernel_decode_gb300.build()) first")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes, fn.restype = args, res
+        _lib = L
+    return _lib
+
+
+class KieError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def _check(rc: int, ctx=None):
+    if rc != KIE_OK:
+        raise KieError(rc, (lib().kie_last_error(ctx) or b"").decode())
+
+
+# ---- thin wrappers with the C names --------------------------------------------------------------------
+
+def make_config(model, max_seq: int) -> KieConfig:
+    return KieConfig(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
+                     model.ffn_dim, model.vocab, max_seq, model.rope_theta, model.rms_eps)
+
+
+def kie_query_buffers(cfg: KieConfig, n_cta: int = 0) -> KieBufferSizes:
+    out = KieBufferSizes()
+    _check(lib().kie_query_buffers(ctypes.byref(cfg), n_cta, ctypes.byref(out)))
+    return out
+
+
+class _HostWeights:
+    """ctypes view of a weights dict (fp16 bit arrays) that keeps every array alive."""
+
+    def __init__(self, weights: dict, n_layers: int):
+        self.keep = weights
+        self.arrays = {}
+        ptrs = {}
+        for name in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
+            arrs = [np.ascontiguousarray(weights["layers"][l][name], dtype=np.uint16) for l in range(n_layers)]
+            self.arrays[name] = arrs
+            tbl = (P * max(n_layers, 1))(*[a.ctypes.data for a in arrs])
+            self.arrays[name + "_tbl"] = tbl
+            ptrs[name] = ctypes.cast(tbl, P)
+        for name in ("embed", "lm_head", "final_norm"):
+            self.arrays[name] = np.ascontiguousarray(weights[name], dtype=np.uint16)
+        self.struct = KieWeights(embed=self.arrays["embed"].ctypes.data, lm_head=self.arrays["lm_head"].ctypes.data,
+                                 final_norm=self.arrays["final_norm"].ctypes.data, **ptrs)
+
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("persistent_monokernel_decode_gb300 needs a CUDA GPU; none is available")
+    return torch
+
+
+class Decoder:
+    """One decode context (kie_ctx): repacked weights, KV cache and workspace in torch-allocated HBM."""
+
+    def __init__(self, model, weights: dict, max_seq: int, stream=None):
+        torch = _torch()
+        self.model, self.max_seq = model, max_seq
+        self.cfg = make_config(model, max_seq)
+        sizes = kie_query_buffers(self.cfg, 0)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        self._wbuf = torch.empty(sizes.weights_bytes, dtype=torch.uint8, device=dev)
+        self._kvbuf = torch.empty(sizes.kv_bytes, dtype=torch.uint8, device=dev)
+        self._wsbuf = torch.empty(sizes.workspace_bytes, dtype=torch.uint8, device=dev)
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        hw = _HostWeights(weights, model.n_layers)
+        ctx = P()
+        rc = lib().kie_create_with_buffers(ctypes.byref(self.cfg), ctypes.byref(hw.struct),
+                                           P(self.stream.cuda_stream), self._wbuf.data_ptr(), sizes.weights_bytes,
+                                           self._kvbuf.data_ptr(), sizes.kv_bytes, self._wsbuf.data_ptr(),
+                                           sizes.workspace_bytes, ctypes.byref(ctx))
+        _check(rc, None)
+        self.ctx = ctx
+        self.n_cta = lib().kie_n_cta(ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().kie_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, tokens) -> None:
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(lib().kie_prefill(self.ctx, t.ctypes.data, t.size), self.ctx)
+
+    def decode(self, n: int) -> np.ndarray:
+        out = np.empty(n, dtype=np.int32)
+        _check(lib().kie_decode(self.ctx, n, out.ctypes.data), self.ctx)
+        return out
+
+    def decode_async(self, n: int, out_dev) -> None:
+        """Enqueue n greedy tokens into the device int32 tensor out_dev; no synchronisation."""
+        _check(lib().kie_decode_async(self.ctx, n, out_dev.data_ptr()), self.ctx)
+
+    def sync(self) -> None:
+        _check(lib().kie_sync(self.ctx), self.ctx)
+
+    def decode_forced(self, forced, want_logits: bool = True):
+        f = np.ascontiguousarray(forced, dtype=np.int32)
+        toks = np.empty(f.size, dtype=np.int32)
+        logits = np.empty((f.size, self.model.vocab), dtype=np.float32) if want_logits else None
+        _check(lib().kie_decode_forced(self.ctx, f.size, f.ctypes.data, toks.ctypes.data,
+                                       logits.ctypes.data if want_logits else None), self.ctx)
+        return toks, logits
+
+    def logits(self) -> np.ndarray:
+        out = np.empty(self.model.vocab, dtype=np.float32)
+        _check(lib().kie_get_logits(self.ctx, out.ctypes.data), self.ctx)
+        return out
+
+    @property
+    def position(self) -> int:
+        return lib().kie_position(self.ctx)
+
+    def reset(self) -> None:
+        _check(lib().kie_reset(self.ctx), self.ctx)
+
+    def set_timeout_ns(self, ns: int) -> None:
+        _check(lib().kie_set_timeout_ns(self.ctx, ns), self.ctx)
+
+    def barrier_stats(self) -> dict:
+        st = KieBarrierStats()
+        _check(lib().kie_get_barrier_stats(self.ctx, ctypes.byref(st)), self.ctx)
+        return {"barriers": st.barriers, "mean_wait_ns": st.mean_wait_ns,
+                "mean_latency_ns": st.mean_latency_ns, "total_ns": st.total_ns}
+
+    def debug_skip_arrival(self, cta: int, barrier: int) -> None:
+        _check(lib().kie_debug_skip_arrival(self.ctx, cta, barrier), self.ctx)
+
+
+# ---- standalone GEMV ----------------------------------------------------------------------------------
+
+def gemv_pack(W, n_cta: int = 0):
+    """Pack a row-major fp16 CUDA tensor W [M, K] into the per-CTA tile layout (returns a new tensor)."""
+    torch = _torch()
+    M, K = W.shape
+    packed = torch.empty(M * K, dtype=torch.int16, device=W.device)
+    _check(lib().kie_gemv_pack(W.data_ptr(), M, K, n_cta, packed.data_ptr(),
+                               P(torch.cuda.current_stream().cuda_stream)))
+    return packed
+
+
+def gemv(packed, x, M: int, K: int, n_cta: int = 0, y=None):
+    """y = W x (fp32) from a packed fp16 W and an fp16 CUDA vector x, on the current stream."""
+    torch = _torch()
+    if y is None:
+        y = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(lib().kie_gemv(packed.data_ptr(), x.data_ptr(), y.data_ptr(), M, K, n_cta,
+                          P(torch.cuda.current_stream().cuda_stream)))
+    return y
+
+
+def packed_offset(M: int, K: int, n_cta: int, r: int, c: int) -> int:
+    return lib().kie_packed_offset(M, K, n_cta, r, c)
+
+
+def rows_of_cta(M: int, n_cta: int, cta: int):
+    r0, r1 = ctypes.c_int(), ctypes.c_int()
+    _check(lib().kie_rows_of_cta(M, n_cta, cta, ctypes.byref(r0), ctypes.byref(r1)))
+    return r0.value, r1.value

@@ -1,0 +1,666 @@
+// C ABI of the decode library (declared in include/kie.h): configuration checks, device buffer planning,
+// the offline weight repack, and the host side of every launch.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kie.h"
+#include "kie_decode.cuh"
+#include "kie_device.cuh"
+
+cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream);
+int kie_decode_max_blocks_per_sm(size_t smem);
+cudaError_t kie_launch_gemv(const uint8_t *packed, const __half *x, float *y, int M, int K, int n_cta, int nslot,
+                            unsigned long long timeout_ns, cudaStream_t stream);
+cudaError_t kie_launch_pack(const uint16_t *src, uint16_t *dst, int M, int K, int n_cta, const uint16_t *gain,
+                            cudaStream_t stream);
+
+namespace {
+
+constexpr int LOGIT_CHUNK = 64;  // forced-decode steps per launch when per-step logits are returned
+constexpr unsigned long long DEFAULT_TIMEOUT_NS = 1000000000ull;
+constexpr size_t ALIGN = 256;
+
+thread_local std::string g_create_error;
+
+size_t al(size_t v) { return kie::align_up(v, ALIGN); }
+
+struct WeightLayout {
+  size_t qkv, wo, gu, down, layer_stride, lm, embed, total;
+};
+
+struct WsLayout {
+  size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, stats, tok_in, tok_out, chunk, total;
+  int smax;
+};
+
+struct Plan {
+  int n_cta, nslot, vec_floats, out_floats;
+  size_t smem;
+  WeightLayout w;
+  WsLayout ws;
+  size_t kv_bytes;
+};
+
+int max_rows_per_cta(int M, int n) { return 2 * ((M / 2 + n - 1) / n); }
+
+const char *check_config(const kie_config *c) {
+  if (!c) return "config is NULL";
+  if (c->n_layers < 1) return "n_layers must be >= 1";
+  if (c->d_model < 8 || c->d_model % 8) return "d_model must be a positive multiple of 8";
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+  if (c->n_heads / c->n_kv_heads > kie::MAX_GROUP) return "more than 8 query heads per KV head";
+  if (c->n_kv_heads > kie::MAX_KV_HEADS) return "more than 64 KV heads";
+  if (c->head_dim != 64 && c->head_dim != 128) return "head_dim must be 64 or 128";
+  if (c->ffn_dim < 8 || c->ffn_dim % 8) return "ffn_dim must be a positive multiple of 8";
+  if (c->vocab < 2 || c->vocab % 2) return "vocab must be even and >= 2";
+  if (c->max_seq < 1) return "max_seq must be >= 1";
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f)) return "rms_eps must be >= 0 and rope_theta > 0";
+  return nullptr;
+}
+
+const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) {
+  const int d = c->d_model, dh = c->head_dim, dq = c->n_heads * dh, G = c->n_heads / c->n_kv_heads;
+  const size_t L = (size_t)c->n_layers;
+  pl->n_cta = n_cta;
+  if (n_cta < c->n_kv_heads) return "the grid needs at least one CTA per KV head";
+  // shared memory: ring + input vector (largest of d, F, Hq*dh, attention scratch) + row results
+  const int att = G * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + kie::NCW * G * dh;
+  pl->vec_floats = std::max(std::max(d, c->ffn_dim), std::max(dq, att));
+  pl->out_floats = std::max(std::max(max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta),
+                                     max_rows_per_cta(d, n_cta)),
+                            std::max(max_rows_per_cta(2 * c->ffn_dim, n_cta), max_rows_per_cta(c->vocab, n_cta)));
+  const size_t fixed = kie::smem_bytes(0, pl->vec_floats, pl->out_floats);
+  const long long room = (long long)smem_optin - (long long)fixed - 1024;
+  int nslot = room > 0 ? (int)(room / (kie::SLOT_BYTES + 16)) : 0;
+  nslot = std::min(nslot, 16);
+  if (nslot < 4) return "model too wide: shared memory leaves fewer than 4 ring slots";
+  pl->nslot = nslot;
+  pl->smem = kie::smem_bytes(nslot, pl->vec_floats, pl->out_floats);
+  // weights
+  WeightLayout &w = pl->w;
+  const size_t qkv = (size_t)(c->n_heads + 2 * c->n_kv_heads) * dh * d * 2;
+  w.qkv = 0;
+  w.wo = al(qkv);
+  w.gu = w.wo + al((size_t)d * dq * 2);
+  w.down = w.gu + al((size_t)2 * c->ffn_dim * d * 2);
+  w.layer_stride = w.down + al((size_t)d * c->ffn_dim * 2);
+  w.lm = L * w.layer_stride;
+  w.embed = w.lm + al((size_t)c->vocab * d * 2);
+  w.total = w.embed + al((size_t)c->vocab * d * 2);
+  // K/V cache
+  pl->kv_bytes = al(L * 2 * c->n_kv_heads * (size_t)c->max_seq * dh * 2);
+  // workspace
+  WsLayout &s = pl->ws;
+  s.smax = std::max(1, n_cta / c->n_kv_heads);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  s.x = take((size_t)d * 4);
+  s.h = take((size_t)d * 4);
+  s.q = take((size_t)dq * 4);
+  s.o = take((size_t)dq * 4);
+  s.a = take((size_t)c->ffn_dim * 4);
+  s.logits = take((size_t)c->vocab * 4);
+  s.part_o = take((size_t)c->n_kv_heads * s.smax * G * dh * 4);
+  s.part_ml = take((size_t)c->n_kv_heads * s.smax * G * 2 * 4);
+  s.rope = take((size_t)c->max_seq * (dh / 2) * 8);
+  s.ctl = take(sizeof(kie::Ctl));
+  s.persist = take(sizeof(kie::Persist));
+  s.trace = take((size_t)kie::TRACE_CAP * n_cta * 4);
+  s.stats = take((size_t)n_cta * 4 * 8);
+  s.tok_in = take((size_t)c->max_seq * 4);
+  s.tok_out = take((size_t)c->max_seq * 4);
+  s.chunk = take((size_t)LOGIT_CHUNK * c->vocab * 4);
+  s.total = o;
+  return nullptr;
+}
+
+struct DeviceInfo {
+  int dev, sms, smem_optin;
+};
+
+bool device_info(DeviceInfo *di, std::string *err) {
+  cudaError_t e = cudaGetDevice(&di->dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di->sms, cudaDevAttrMultiProcessorCount, di->dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&di->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, di->dev);
+  if (e != cudaSuccess) {
+    *err = std::string("CUDA device query failed: ") + cudaGetErrorString(e);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+struct kie_ctx {
+  kie_config cfg{};
+  cudaStream_t stream = nullptr;
+  Plan plan{};
+  bool owns = false;
+  uint8_t *wbuf = nullptr, *kvbuf = nullptr, *wsbuf = nullptr;
+  kie::DecodeParams base{};
+  int pos = 0;
+  bool has_logits = false;
+  unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
+  int skip_cta = -1, skip_barrier = -1;
+  int32_t *pinned = nullptr;  // host staging: [max_seq] tokens + status words
+  std::string err;
+};
+
+namespace {
+
+int fail(kie_ctx *ctx, int code, const std::string &msg) {
+  if (ctx)
+    ctx->err = msg;
+  else
+    g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(kie_ctx *ctx, cudaError_t e, const char *what) {
+  return fail(ctx, KIE_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define KIE_CUDA(ctx, call)                                  \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+  } while (0)
+
+// Host copy of the fused QKV matrix: every query and key head becomes dh/2 row pairs (i, i + dh/2), so that
+// one CTA holds both inputs of each RoPE rotation; value heads are copied as they are.
+void fuse_qkv(const kie_config &c, const uint16_t *wq, const uint16_t *wk, const uint16_t *wv, uint16_t *dst) {
+  const int d = c.d_model, dh = c.head_dim, half = dh / 2;
+  const size_t row = (size_t)d;
+  auto pairs = [&](const uint16_t *src, int heads) {
+    for (int h = 0; h < heads; ++h)
+      for (int i = 0; i < half; ++i) {
+        std::memcpy(dst, src + ((size_t)h * dh + i) * row, row * 2);
+        dst += row;
+        std::memcpy(dst, src + ((size_t)h * dh + i + half) * row, row * 2);
+        dst += row;
+      }
+  };
+  pairs(wq, c.n_heads);
+  pairs(wk, c.n_kv_heads);
+  std::memcpy(dst, wv, (size_t)c.n_kv_heads * dh * row * 2);
+}
+
+// Host copy of the gate/up matrix with rows interleaved: row 2j = gate_j, row 2j+1 = up_j.
+void fuse_gate_up(const kie_config &c, const uint16_t *wg, const uint16_t *wu, uint16_t *dst) {
+  const size_t row = (size_t)c.d_model;
+  for (int j = 0; j < c.ffn_dim; ++j) {
+    std::memcpy(dst + (2 * (size_t)j) * row, wg + (size_t)j * row, row * 2);
+    std::memcpy(dst + (2 * (size_t)j + 1) * row, wu + (size_t)j * row, row * 2);
+  }
+}
+
+int upload_and_pack(kie_ctx *ctx, const uint16_t *host, int M, int K, uint8_t *dst, const uint16_t *gain_host,
+                    uint16_t *stage, uint16_t *gain_dev) {
+  const size_t bytes = (size_t)M * K * 2;
+  KIE_CUDA(ctx, cudaMemcpyAsync(stage, host, bytes, cudaMemcpyHostToDevice, ctx->stream));
+  const uint16_t *g = nullptr;
+  if (gain_host) {
+    KIE_CUDA(ctx, cudaMemcpyAsync(gain_dev, gain_host, (size_t)K * 2, cudaMemcpyHostToDevice, ctx->stream));
+    g = gain_dev;
+  }
+  KIE_CUDA(ctx, kie_launch_pack(stage, (uint16_t *)dst, M, K, ctx->plan.n_cta, g, ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  return KIE_OK;
+}
+
+int repack_weights(kie_ctx *ctx, const kie_weights *w) {
+  const kie_config &c = ctx->cfg;
+  const Plan &pl = ctx->plan;
+  const int d = c.d_model, dh = c.head_dim, dq = c.n_heads * dh, F = c.ffn_dim;
+  const int Mqkv = (c.n_heads + 2 * c.n_kv_heads) * dh;
+  const size_t stage_elems = std::max({(size_t)Mqkv * d, (size_t)d * dq, (size_t)2 * F * d, (size_t)c.vocab * d});
+  uint16_t *stage = nullptr, *gain = nullptr;
+  cudaError_t e = cudaMalloc(&stage, stage_elems * 2);
+  if (e != cudaSuccess) return fail(ctx, KIE_ERR_OOM, "staging buffer for the repack: out of device memory");
+  e = cudaMalloc(&gain, (size_t)std::max(d, F) * 2);
+  if (e != cudaSuccess) {
+    cudaFree(stage);
+    return fail(ctx, KIE_ERR_OOM, "staging buffer for the repack: out of device memory");
+  }
+  std::vector<uint16_t> host(std::max((size_t)Mqkv * d, (size_t)2 * F * d));
+  int rc = KIE_OK;
+  for (int l = 0; l < c.n_layers && rc == KIE_OK; ++l) {
+    uint8_t *lw = ctx->wbuf + (size_t)l * pl.w.layer_stride;
+    fuse_qkv(c, w->wq[l], w->wk[l], w->wv[l], host.data());
+    rc = upload_and_pack(ctx, host.data(), Mqkv, d, lw + pl.w.qkv, w->attn_norm[l], stage, gain);
+    if (rc == KIE_OK) rc = upload_and_pack(ctx, w->wo[l], d, dq, lw + pl.w.wo, nullptr, stage, gain);
+    if (rc == KIE_OK) {
+      fuse_gate_up(c, w->w_gate[l], w->w_up[l], host.data());
+      rc = upload_and_pack(ctx, host.data(), 2 * F, d, lw + pl.w.gu, w->ffn_norm[l], stage, gain);
+    }
+    if (rc == KIE_OK) rc = upload_and_pack(ctx, w->w_down[l], d, F, lw + pl.w.down, nullptr, stage, gain);
+  }
+  if (rc == KIE_OK) rc = upload_and_pack(ctx, w->lm_head, c.vocab, d, ctx->wbuf + pl.w.lm, w->final_norm, stage, gain);
+  if (rc == KIE_OK) {
+    e = cudaMemcpyAsync(ctx->wbuf + pl.w.embed, w->embed, (size_t)c.vocab * d * 2, cudaMemcpyHostToDevice, ctx->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) rc = cuda_fail(ctx, e, "embedding upload");
+  }
+  cudaFree(stage);
+  cudaFree(gain);
+  return rc;
+}
+
+// RoPE table: row p holds (cos, sin) of p * theta^(-2i/dh) for i < dh/2, evaluated in fp64, stored fp32.
+int upload_rope(kie_ctx *ctx) {
+  const kie_config &c = ctx->cfg;
+  const int half = c.head_dim / 2;
+  std::vector<float> tab((size_t)c.max_seq * half * 2);
+  for (int i = 0; i < half; ++i) {
+    const double inv_freq = std::exp(-2.0 * i / c.head_dim * std::log((double)c.rope_theta));
+    for (int p = 0; p < c.max_seq; ++p) {
+      const double ang = (double)p * inv_freq;
+      tab[((size_t)p * half + i) * 2] = (float)std::cos(ang);
+      tab[((size_t)p * half + i) * 2 + 1] = (float)std::sin(ang);
+    }
+  }
+  KIE_CUDA(ctx, cudaMemcpyAsync(ctx->wsbuf + ctx->plan.ws.rope, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice,
+                                ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  return KIE_OK;
+}
+
+void fill_base(kie_ctx *ctx) {
+  const kie_config &c = ctx->cfg;
+  const Plan &pl = ctx->plan;
+  kie::DecodeParams &p = ctx->base;
+  std::memset(&p, 0, sizeof(p));
+  p.L = c.n_layers;
+  p.d = c.d_model;
+  p.Hq = c.n_heads;
+  p.Hkv = c.n_kv_heads;
+  p.dh = c.head_dim;
+  p.F = c.ffn_dim;
+  p.V = c.vocab;
+  p.max_seq = c.max_seq;
+  p.n_cta = pl.n_cta;
+  p.nslot = pl.nslot;
+  p.vec_floats = pl.vec_floats;
+  p.out_floats = pl.out_floats;
+  p.eps = c.rms_eps;
+  p.wbase = ctx->wbuf;
+  p.layer_stride = (long long)pl.w.layer_stride;
+  p.off_qkv = (long long)pl.w.qkv;
+  p.off_wo = (long long)pl.w.wo;
+  p.off_gu = (long long)pl.w.gu;
+  p.off_down = (long long)pl.w.down;
+  p.w_lm = ctx->wbuf + pl.w.lm;
+  p.embed = (const __half *)(ctx->wbuf + pl.w.embed);
+  p.kv = (__half *)ctx->kvbuf;
+  uint8_t *ws = ctx->wsbuf;
+  p.rope = (const float2 *)(ws + pl.ws.rope);
+  p.x = (float *)(ws + pl.ws.x);
+  p.h = (float *)(ws + pl.ws.h);
+  p.q = (float *)(ws + pl.ws.q);
+  p.o = (float *)(ws + pl.ws.o);
+  p.a = (float *)(ws + pl.ws.a);
+  p.logits = (float *)(ws + pl.ws.logits);
+  p.part_o = (float *)(ws + pl.ws.part_o);
+  p.part_ml = (float *)(ws + pl.ws.part_ml);
+  p.smax = pl.ws.smax;
+  p.ctl = (kie::Ctl *)(ws + pl.ws.ctl);
+  p.persist = (kie::Persist *)(ws + pl.ws.persist);
+  p.trace = (uint32_t *)(ws + pl.ws.trace);
+  p.cta_stats = (unsigned long long *)(ws + pl.ws.stats);
+  p.skip_cta = -1;
+  p.skip_barrier = -1;
+}
+
+int create_common(const kie_config *cfg, const kie_weights *w, void *stream, void *wdev, size_t wbytes, void *kvdev,
+                  size_t kvbytes, void *wsdev, size_t wsbytes, kie_ctx **out) {
+  if (!out) return fail(nullptr, KIE_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (const char *m = check_config(cfg)) return fail(nullptr, KIE_ERR_INVALID, m);
+  if (!w || !w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+      !w->ffn_norm || !w->w_gate || !w->w_up || !w->w_down)
+    return fail(nullptr, KIE_ERR_INVALID, "a weight pointer is NULL");
+  for (int l = 0; l < cfg->n_layers; ++l)
+    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->ffn_norm[l] || !w->w_gate[l] ||
+        !w->w_up[l] || !w->w_down[l])
+      return fail(nullptr, KIE_ERR_INVALID, "a per-layer weight pointer is NULL");
+  DeviceInfo di;
+  std::string err;
+  if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
+  kie_ctx *ctx = new kie_ctx();
+  ctx->cfg = *cfg;
+  ctx->stream = (cudaStream_t)stream;
+  if (const char *m = make_plan(cfg, di.sms, di.smem_optin, &ctx->plan)) {
+    delete ctx;
+    return fail(nullptr, KIE_ERR_INVALID, m);
+  }
+  const int nb = kie_decode_max_blocks_per_sm(ctx->plan.smem);
+  if (nb < 1) {
+    delete ctx;
+    return fail(nullptr, KIE_ERR_LAUNCH, "the decode kernel cannot be resident with its shared memory");
+  }
+  const Plan &pl = ctx->plan;
+  if (wdev) {
+    if (wbytes < pl.w.total || kvbytes < pl.kv_bytes || wsbytes < pl.ws.total || ((uintptr_t)wdev % ALIGN) ||
+        ((uintptr_t)kvdev % ALIGN) || ((uintptr_t)wsdev % ALIGN)) {
+      delete ctx;
+      return fail(nullptr, KIE_ERR_INVALID, "a caller buffer is too small or not 256-byte aligned");
+    }
+    ctx->wbuf = (uint8_t *)wdev;
+    ctx->kvbuf = (uint8_t *)kvdev;
+    ctx->wsbuf = (uint8_t *)wsdev;
+  } else {
+    ctx->owns = true;
+    if (cudaMalloc(&ctx->wbuf, pl.w.total) != cudaSuccess || cudaMalloc(&ctx->kvbuf, pl.kv_bytes) != cudaSuccess ||
+        cudaMalloc(&ctx->wsbuf, pl.ws.total) != cudaSuccess) {
+      cudaGetLastError();
+      kie_destroy(ctx);
+      return fail(nullptr, KIE_ERR_OOM, "device allocation failed");
+    }
+  }
+  if (cudaMallocHost(&ctx->pinned, ((size_t)cfg->max_seq + 64) * 4) != cudaSuccess) {
+    cudaGetLastError();
+    kie_destroy(ctx);
+    return fail(nullptr, KIE_ERR_OOM, "pinned host allocation failed");
+  }
+  int rc = KIE_OK;
+  cudaError_t e = cudaMemsetAsync(ctx->kvbuf, 0, pl.kv_bytes, ctx->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->wsbuf, 0, pl.ws.total, ctx->stream);
+  if (e != cudaSuccess) rc = cuda_fail(ctx, e, "clearing device buffers");
+  if (rc == KIE_OK) rc = repack_weights(ctx, w);
+  if (rc == KIE_OK) rc = upload_rope(ctx);
+  if (rc != KIE_OK) {
+    g_create_error = ctx->err;
+    kie_destroy(ctx);
+    return rc;
+  }
+  fill_base(ctx);
+  *out = ctx;
+  return KIE_OK;
+}
+
+// One launch of the decode kernel. forced_dev / out_tokens_dev / out_logits_dev may be null.
+int launch(kie_ctx *ctx, int n, int mode, int lm_last_only, const int *forced_dev, int *out_tokens_dev,
+           float *out_logits_dev) {
+  kie::DecodeParams p = ctx->base;
+  p.pos0 = ctx->pos;
+  p.n = n;
+  p.mode = mode;
+  p.lm_last_only = lm_last_only;
+  p.forced = forced_dev;
+  p.out_tokens = out_tokens_dev;
+  p.out_logits = out_logits_dev;
+  p.timeout_ns = ctx->timeout_ns;
+  p.skip_cta = ctx->skip_cta;
+  p.skip_barrier = ctx->skip_barrier;
+  ctx->skip_cta = ctx->skip_barrier = -1;
+  const Plan &pl = ctx->plan;
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + pl.ws.ctl, 0, sizeof(kie::Ctl), ctx->stream));
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + pl.ws.stats, 0, (size_t)pl.n_cta * 32, ctx->stream));
+  cudaError_t e = kie_launch_decode(p, pl.smem, ctx->stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return fail(ctx, KIE_ERR_LAUNCH, "cooperative launch refused: the grid cannot be co-resident");
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "decode kernel launch");
+  ctx->pos += n;
+  return KIE_OK;
+}
+
+// Wait for the stream and read the status word of the last launch.
+int finish(kie_ctx *ctx) {
+  int32_t *st = ctx->pinned + ctx->cfg.max_seq;
+  KIE_CUDA(ctx, cudaMemcpyAsync(st, ctx->wsbuf + ctx->plan.ws.ctl + offsetof(kie::Ctl, status), 8,
+                                cudaMemcpyDeviceToHost, ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  if (st[0] != kie::ST_OK) {
+    ctx->pos = 0;
+    ctx->has_logits = false;
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "device wait timed out (status %d, first timed-out barrier %d); sequence reset",
+                  st[0], st[1] - 1);
+    return fail(ctx, KIE_ERR_TIMEOUT, buf);
+  }
+  return KIE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kie_query_buffers(const kie_config *cfg, int n_cta, kie_buffer_sizes *out) {
+  if (!out) return KIE_ERR_INVALID;
+  if (const char *m = check_config(cfg)) return fail(nullptr, KIE_ERR_INVALID, m);
+  DeviceInfo di{0, n_cta, 232448};
+  std::string err;
+  if (n_cta <= 0) {
+    if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
+  }
+  Plan pl;
+  if (const char *m = make_plan(cfg, di.sms, di.smem_optin, &pl)) return fail(nullptr, KIE_ERR_INVALID, m);
+  out->weights_bytes = pl.w.total;
+  out->kv_bytes = pl.kv_bytes;
+  out->workspace_bytes = pl.ws.total;
+  out->n_cta = pl.n_cta;
+  return KIE_OK;
+}
+
+int kie_create(const kie_config *cfg, const kie_weights *w, void *stream, kie_ctx **out) {
+  return create_common(cfg, w, stream, nullptr, 0, nullptr, 0, nullptr, 0, out);
+}
+
+int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *stream, void *weights_dev,
+                            size_t weights_bytes, void *kv_dev, size_t kv_bytes, void *workspace_dev,
+                            size_t workspace_bytes, kie_ctx **out) {
+  if (!weights_dev || !kv_dev || !workspace_dev) return fail(nullptr, KIE_ERR_INVALID, "a device buffer is NULL");
+  return create_common(cfg, w, stream, weights_dev, weights_bytes, kv_dev, kv_bytes, workspace_dev, workspace_bytes,
+                       out);
+}
+
+int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (!tokens || n < 1) return fail(ctx, KIE_ERR_INVALID, "prefill needs n >= 1 tokens");
+  if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "prompt exceeds max_seq");
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= ctx->cfg.vocab) return fail(ctx, KIE_ERR_INVALID, "token id out of range");
+  std::memcpy(ctx->pinned, tokens, (size_t)n * 4);
+  int *tin = (int *)(ctx->wsbuf + ctx->plan.ws.tok_in);
+  KIE_CUDA(ctx, cudaMemcpyAsync(tin, ctx->pinned, (size_t)n * 4, cudaMemcpyHostToDevice, ctx->stream));
+  int rc = launch(ctx, n, kie::MODE_FORCED, 1, tin, nullptr, nullptr);
+  if (rc == KIE_OK) rc = finish(ctx);
+  if (rc == KIE_OK) ctx->has_logits = true;
+  return rc;
+}
+
+int kie_decode_async(kie_ctx *ctx, int n, int32_t *out_tokens_dev) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (n < 1 || !out_tokens_dev) return fail(ctx, KIE_ERR_INVALID, "decode needs n >= 1 and an output buffer");
+  if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
+  if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
+  return launch(ctx, n, kie::MODE_DECODE, 0, nullptr, out_tokens_dev, nullptr);
+}
+
+int kie_sync(kie_ctx *ctx) {
+  if (!ctx) return KIE_ERR_INVALID;
+  return finish(ctx);
+}
+
+int kie_decode(kie_ctx *ctx, int n, int32_t *out_tokens) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (!out_tokens) return fail(ctx, KIE_ERR_INVALID, "out_tokens is NULL");
+  int *tout = (int *)(ctx->wsbuf + ctx->plan.ws.tok_out);
+  int rc = kie_decode_async(ctx, n, tout);
+  if (rc != KIE_OK) return rc;
+  KIE_CUDA(ctx, cudaMemcpyAsync(ctx->pinned, tout, (size_t)n * 4, cudaMemcpyDeviceToHost, ctx->stream));
+  rc = finish(ctx);
+  if (rc == KIE_OK) std::memcpy(out_tokens, ctx->pinned, (size_t)n * 4);
+  return rc;
+}
+
+int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_tokens, float *out_logits) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (n < 1 || !forced || !out_tokens) return fail(ctx, KIE_ERR_INVALID, "forced decode needs n >= 1 and buffers");
+  if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
+  if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
+  for (int i = 0; i < n; ++i)
+    if (forced[i] < 0 || forced[i] >= ctx->cfg.vocab) return fail(ctx, KIE_ERR_INVALID, "token id out of range");
+  const int V = ctx->cfg.vocab;
+  int *tin = (int *)(ctx->wsbuf + ctx->plan.ws.tok_in);
+  int *tout = (int *)(ctx->wsbuf + ctx->plan.ws.tok_out);
+  float *chunk = (float *)(ctx->wsbuf + ctx->plan.ws.chunk);
+  for (int done = 0; done < n;) {
+    const int m = std::min(LOGIT_CHUNK, n - done);
+    std::memcpy(ctx->pinned, forced + done, (size_t)m * 4);
+    KIE_CUDA(ctx, cudaMemcpyAsync(tin, ctx->pinned, (size_t)m * 4, cudaMemcpyHostToDevice, ctx->stream));
+    int rc = launch(ctx, m, kie::MODE_FORCED, 0, tin, tout, out_logits ? chunk : nullptr);
+    if (rc != KIE_OK) return rc;
+    KIE_CUDA(ctx, cudaMemcpyAsync(out_tokens + done, tout, (size_t)m * 4, cudaMemcpyDeviceToHost, ctx->stream));
+    if (out_logits)
+      KIE_CUDA(ctx, cudaMemcpyAsync(out_logits + (size_t)done * V, chunk, (size_t)m * V * 4, cudaMemcpyDeviceToHost,
+                                    ctx->stream));
+    rc = finish(ctx);
+    if (rc != KIE_OK) return rc;
+    done += m;
+  }
+  return KIE_OK;
+}
+
+int kie_get_logits(kie_ctx *ctx, float *out) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (!out) return fail(ctx, KIE_ERR_INVALID, "out is NULL");
+  if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "no current logits");
+  KIE_CUDA(ctx, cudaMemcpyAsync(out, ctx->wsbuf + ctx->plan.ws.logits, (size_t)ctx->cfg.vocab * 4,
+                                cudaMemcpyDeviceToHost, ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  return KIE_OK;
+}
+
+int kie_position(const kie_ctx *ctx) { return ctx ? ctx->pos : KIE_ERR_INVALID; }
+
+int kie_reset(kie_ctx *ctx) {
+  if (!ctx) return KIE_ERR_INVALID;
+  ctx->pos = 0;
+  ctx->has_logits = false;
+  return KIE_OK;
+}
+
+int kie_set_timeout_ns(kie_ctx *ctx, uint64_t ns) {
+  if (!ctx || ns == 0) return KIE_ERR_INVALID;
+  ctx->timeout_ns = ns;
+  return KIE_OK;
+}
+
+int kie_get_barrier_stats(kie_ctx *ctx, kie_barrier_stats *out) {
+  if (!ctx || !out) return KIE_ERR_INVALID;
+  const Plan &pl = ctx->plan;
+  const int n = pl.n_cta;
+  std::vector<unsigned long long> st((size_t)n * 4);
+  KIE_CUDA(ctx, cudaMemcpyAsync(st.data(), ctx->wsbuf + pl.ws.stats, st.size() * 8, cudaMemcpyDeviceToHost, ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  const long long bars = (long long)st[1];
+  const int traced = (int)std::min<long long>(bars, kie::TRACE_CAP);
+  std::vector<uint32_t> tr((size_t)std::max(traced, 1) * n);
+  if (traced > 0) {
+    KIE_CUDA(ctx, cudaMemcpyAsync(tr.data(), ctx->wsbuf + pl.ws.trace, (size_t)traced * n * 4, cudaMemcpyDeviceToHost,
+                                  ctx->stream));
+    KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  }
+  double wait = 0, cnt = 0, lat = 0;
+  for (int i = 0; i < n; ++i) {
+    wait += (double)st[(size_t)i * 4];
+    cnt += (double)st[(size_t)i * 4 + 1];
+  }
+  for (int b = 0; b < traced; ++b) {
+    uint32_t m = 0xFFFFFFFFu;
+    for (int i = 0; i < n; ++i) m = std::min(m, tr[(size_t)b * n + i]);
+    lat += m;
+  }
+  out->barriers = bars;
+  out->mean_wait_ns = cnt > 0 ? wait / cnt : 0.0;
+  out->mean_latency_ns = traced > 0 ? lat / traced : 0.0;
+  out->total_ns = (double)(st[3] - st[2]);
+  return KIE_OK;
+}
+
+int kie_debug_skip_arrival(kie_ctx *ctx, int cta, int barrier) {
+  if (!ctx) return KIE_ERR_INVALID;
+  ctx->skip_cta = cta;
+  ctx->skip_barrier = barrier;
+  return KIE_OK;
+}
+
+int kie_n_cta(const kie_ctx *ctx) { return ctx ? ctx->plan.n_cta : KIE_ERR_INVALID; }
+
+const char *kie_last_error(const kie_ctx *ctx) { return ctx ? ctx->err.c_str() : g_create_error.c_str(); }
+
+void kie_destroy(kie_ctx *ctx) {
+  if (!ctx) return;
+  if (ctx->stream || ctx->wbuf) cudaStreamSynchronize(ctx->stream);
+  if (ctx->owns) {
+    cudaFree(ctx->wbuf);
+    cudaFree(ctx->kvbuf);
+    cudaFree(ctx->wsbuf);
+  }
+  if (ctx->pinned) cudaFreeHost(ctx->pinned);
+  delete ctx;
+}
+
+size_t kie_gemv_packed_bytes(int M, int K) { return (size_t)M * K * 2; }
+
+static int gemv_ncta(int n_cta) {
+  if (n_cta > 0) return n_cta;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return sms;
+}
+
+int kie_gemv_pack(const uint16_t *W_dev, int M, int K, int n_cta, uint16_t *packed_dev, void *stream) {
+  if (!W_dev || !packed_dev || M < 2 || M % 2 || K < 8 || K % 8) return fail(nullptr, KIE_ERR_INVALID, "bad GEMV shape");
+  if (((uintptr_t)W_dev | (uintptr_t)packed_dev) % 16) return fail(nullptr, KIE_ERR_INVALID, "unaligned buffer");
+  const int n = gemv_ncta(n_cta);
+  if (n < 1) return fail(nullptr, KIE_ERR_CUDA, "device query failed");
+  cudaError_t e = kie_launch_pack(W_dev, packed_dev, M, K, n, nullptr, (cudaStream_t)stream);
+  return e == cudaSuccess ? KIE_OK : fail(nullptr, KIE_ERR_CUDA, cudaGetErrorString(e));
+}
+
+int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, int M, int K, int n_cta, void *stream) {
+  if (!packed_dev || !x_dev || !y_dev || M < 2 || M % 2 || K < 8 || K % 8) return fail(nullptr, KIE_ERR_INVALID, "bad GEMV shape");
+  if (((uintptr_t)packed_dev | (uintptr_t)x_dev | (uintptr_t)y_dev) % 16) return fail(nullptr, KIE_ERR_INVALID, "unaligned buffer");
+  DeviceInfo di;
+  std::string err;
+  if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
+  const int n = n_cta > 0 ? n_cta : di.sms;
+  const int out_floats = max_rows_per_cta(M, n) + 2;
+  const size_t fixed = kie::smem_bytes(0, K, out_floats);
+  const long long room = (long long)di.smem_optin - (long long)fixed - 1024;
+  const int nslot = std::min(16, room > 0 ? (int)(room / (kie::SLOT_BYTES + 16)) : 0);
+  if (nslot < 2) return fail(nullptr, KIE_ERR_INVALID, "K too large for the shared-memory input vector");
+  cudaError_t e = kie_launch_gemv((const uint8_t *)packed_dev, (const __half *)x_dev, y_dev, M, K, n, nslot,
+                                  DEFAULT_TIMEOUT_NS, (cudaStream_t)stream);
+  return e == cudaSuccess ? KIE_OK : fail(nullptr, KIE_ERR_CUDA, cudaGetErrorString(e));
+}
+
+int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c) {
+  if (M < 2 || M % 2 || K < 1 || n_cta < 1 || r < 0 || r >= M || c < 0 || c >= K) return -1;
+  return kie::packed_offset(M, K, n_cta, r, c);
+}
+
+int kie_rows_of_cta(int M, int n_cta, int cta, int *r0, int *r1) {
+  if (M < 2 || M % 2 || n_cta < 1 || cta < 0 || cta >= n_cta || !r0 || !r1) return KIE_ERR_INVALID;
+  const kie::RowRange r = kie::rows_of_cta(M, n_cta, cta);
+  *r0 = r.r0;
+  *r1 = r.r1;
+  return KIE_OK;
+}
+
+}  // extern "C"

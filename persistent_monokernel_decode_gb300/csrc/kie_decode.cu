@@ -1,0 +1,451 @@
+// The persistent decode monokernel for sm_103a.
+//
+// One cooperative launch of n_cta CTAs (one per SM) runs n whole decode steps, as the monokernel pages
+// describe it ("inside the monokernel": one resident grid runs the token loop, sampling included, and never
+// hands control back to the host between tokens). Per token:
+//
+//   embed -> for each layer:
+//     [QKV]   q,k,v = inv_rms(x) * (W'qkv x); RoPE from the table; K,V appended (fp16) ........ barrier
+//     [ATT]   split-KV attention over the cached positions; the last piece per KV head merges ... barrier
+//     [WO]    h = x + Wo o ........................................................................ barrier
+//     [GU]    a = silu(gate) * up,  [gate; up] = inv_rms(h) * (W'gu h), rows interleaved ........ barrier
+//     [DOWN]  x = h + Wd a ........................................................................ barrier
+//   [LM] logits = inv_rms(x) * (W'lm x); per-CTA argmax folded with one 64-bit atomicMax ........... barrier
+//
+// W' are the repacked weights with the RMSNorm gain folded into their columns (the "RMSNorm folding" and
+// "offline QKV repacking" items of the pages), so a norm is just one scalar computed redundantly by every
+// CTA from the full vector. Weights stream through each CTA's shared-memory ring (kie_device.cuh) without
+// ever waiting for a barrier; consumers wait at the grid barrier, which is one global counter polled with
+// acquire loads and bounded by a %globaltimer limit.
+#include <cuda_runtime.h>
+
+#include "kie_decode.cuh"
+#include "kie_device.cuh"
+
+namespace kie {
+
+// ---- grid barrier -----------------------------------------------------------------------------------------
+
+// All consumer threads of every CTA call this together. Returns false (uniformly within the CTA) when the
+// launch is being abandoned: a wait ran out here or anywhere else.
+__device__ inline bool grid_barrier(const DecodeParams &p, Smem &s, uint32_t &gen, const Guard &g,
+                                    unsigned long long &wait_ns) {
+  consumer_sync();
+  const uint32_t idx = gen++;
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = globaltimer();
+    bool ok = s.flags[0] == 0;
+    if (ok) {
+      __threadfence();  // release this CTA's writes (ordered before by the consumer_sync above)
+      if (!((int)blockIdx.x == p.skip_cta && (int)idx == p.skip_barrier)) atomicAdd(&p.ctl->bar_count, 1u);
+      const unsigned target = (idx + 1u) * (unsigned)p.n_cta;
+      for (int spins = 1;; ++spins) {
+        const unsigned cur = ld_acquire_gpu(&p.ctl->bar_count);
+        if ((int)(cur - target) >= 0) break;
+        if ((spins & 15) == 0) {
+          if (ld_relaxed_gpu(&p.ctl->status) != ST_OK) {
+            ok = false;
+            break;
+          }
+          if (globaltimer() - t0 > p.timeout_ns) {
+            raise_status(g, ST_TIMEOUT);
+            atomicCAS(&p.ctl->where, 0, (int)idx + 1);
+            ok = false;
+            break;
+          }
+        }
+      }
+      __threadfence();
+    }
+    const uint64_t dt = globaltimer() - t0;
+    wait_ns += dt;
+    if (idx < (uint32_t)TRACE_CAP) p.trace[(size_t)idx * p.n_cta + blockIdx.x] = (uint32_t)min(dt, (uint64_t)0xFFFFFFFFu);
+    if (!ok) s.flags[0] = 1;
+  }
+  consumer_sync();
+  return s.flags[0] == 0;
+}
+
+// ---- epilogues ------------------------------------------------------------------------------------------
+
+// Fused QKV rows of this CTA, [r0, r1): rows come in pairs. Query and key pairs hold the two halves
+// (i, i + dh/2) of one RoPE rotation, rotated here with the table row of `pos`; keys and values go to the
+// cache as fp16, queries to p.q (fp32, same pair-adjacent order as the cached keys).
+__device__ inline void epilogue_qkv(const DecodeParams &p, const Smem &s, int l, int pos, int r0, int r1) {
+  const int dh = p.dh, qrows = p.Hq * dh, krows = p.Hkv * dh;
+  const size_t plane = (size_t)p.max_seq * dh;
+  __half *Kl = p.kv + (size_t)l * 2 * p.Hkv * plane;
+  __half *Vl = Kl + (size_t)p.Hkv * plane;
+  const float2 *tab = p.rope + (size_t)pos * (dh / 2);
+  for (int pr = threadIdx.x; pr < (r1 - r0) / 2; pr += NCT) {
+    const int r = r0 + 2 * pr;
+    float a = s.out[2 * pr], b = s.out[2 * pr + 1];
+    if (r < qrows + krows) {
+      const int rr = r < qrows ? r : r - qrows;
+      const float2 cs = tab[(rr % dh) / 2];
+      const float a2 = a * cs.x - b * cs.y, b2 = b * cs.x + a * cs.y;
+      if (r < qrows) {
+        *reinterpret_cast<float2 *>(p.q + r) = make_float2(a2, b2);
+      } else {
+        __half2 kv2 = __floats2half2_rn(a2, b2);
+        *reinterpret_cast<__half2 *>(Kl + (size_t)(rr / dh) * plane + (size_t)pos * dh + rr % dh) = kv2;
+      }
+    } else {
+      const int rr = r - qrows - krows;
+      *reinterpret_cast<__half2 *>(Vl + (size_t)(rr / dh) * plane + (size_t)pos * dh + rr % dh) =
+          __floats2half2_rn(a, b);
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+  const unsigned u = __float_as_uint(v);
+  const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)idx);
+}
+
+__device__ __forceinline__ int key_index(unsigned long long key) {
+  return (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
+}
+
+// ---- split-KV attention -----------------------------------------------------------------------------------
+
+// Piece `sp` of KV head `g`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial
+// (m, l, o) of each of the `group` query heads; the last piece of head g to finish merges all pieces
+// (log-sum-exp rescaling) into p.o. This is the pages' "attention recompute" idea in GB300 form: each SM
+// recomputes exactly its slice from the cache instead of exchanging intermediate attention state.
+template <int DPL>
+__device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, int g, int sp, int S, int j0,
+                                       int j1) {
+  constexpr int DH = DPL * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.Hq / p.Hkv;
+  float *qs = s.vec;                      // [G][DH]
+  float *ps = qs + G * DH;                // [G][ATT_SUB]
+  float *corr = ps + G * ATT_SUB;         // [G]
+  float *mrun = corr + MAX_GROUP;         // [G]
+  float *lrun = mrun + MAX_GROUP;         // [G]
+  float *red = lrun + MAX_GROUP;          // [NCW][G][DH]
+  const float scale = 1.0f / sqrtf((float)DH);
+
+  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i);
+  if (tid < G) {
+    mrun[tid] = -INFINITY;
+    lrun[tid] = 0.f;
+  }
+  consumer_sync();
+
+  const size_t plane = (size_t)p.max_seq * DH;
+  const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + g) * plane;
+  const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + g) * plane;
+
+  float acc[MAX_GROUP][DPL];
+#pragma unroll
+  for (int h = 0; h < MAX_GROUP; ++h)
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+
+  for (int jb = j0; jb < j1; jb += ATT_SUB) {
+    const int nb = min(ATT_SUB, j1 - jb);
+    // scores s = q . k / sqrt(dh): one warp per position, DPL dims per lane
+    for (int jj = warp; jj < nb; jj += NCW) {
+      const __half *kr = Kb + (size_t)(jb + jj) * DH + lane * DPL;
+      float kf[DPL];
+      if constexpr (DPL == 4) {
+        const uint2 raw = __ldcg(reinterpret_cast<const uint2 *>(kr));
+        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        kf[0] = k0.x; kf[1] = k0.y; kf[2] = k1.x; kf[3] = k1.y;
+      } else {
+        const unsigned raw = __ldcg(reinterpret_cast<const unsigned *>(kr));
+        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
+        kf[0] = k0.x; kf[1] = k0.y;
+      }
+#pragma unroll
+      for (int h = 0; h < MAX_GROUP; ++h) {
+        if (h < G) {
+          float d = 0.f;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) d = fmaf(kf[e], qs[h * DH + lane * DPL + e], d);
+          d = warp_sum(d);
+          if (lane == 0) ps[h * ATT_SUB + jj] = d * scale;
+        }
+      }
+    }
+    consumer_sync();
+    // online softmax: one warp per query head
+    for (int h = warp; h < G; h += NCW) {
+      float mx = -INFINITY;
+      for (int jj = lane; jj < nb; jj += 32) mx = fmaxf(mx, ps[h * ATT_SUB + jj]);
+      mx = warp_max(mx);
+      const float mnew = fmaxf(mrun[h], mx);
+      float sum = 0.f;
+      for (int jj = lane; jj < nb; jj += 32) {
+        const float e = expf(ps[h * ATT_SUB + jj] - mnew);
+        ps[h * ATT_SUB + jj] = e;
+        sum += e;
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) {
+        const float c = expf(mrun[h] - mnew);
+        corr[h] = c;
+        lrun[h] = lrun[h] * c + sum;
+        mrun[h] = mnew;
+      }
+    }
+    consumer_sync();
+    // o += p v, after rescaling what this warp accumulated so far
+#pragma unroll
+    for (int h = 0; h < MAX_GROUP; ++h)
+      if (h < G) {
+        const float c = corr[h];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[h][e] *= c;
+      }
+    for (int jj = warp; jj < nb; jj += NCW) {
+      const __half *vr = Vb + (size_t)(jb + jj) * DH + lane * DPL;
+      float vf[DPL];
+      if constexpr (DPL == 4) {
+        const uint2 raw = __ldcg(reinterpret_cast<const uint2 *>(vr));
+        const float2 v0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 v1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        vf[0] = v0.x; vf[1] = v0.y; vf[2] = v1.x; vf[3] = v1.y;
+      } else {
+        const unsigned raw = __ldcg(reinterpret_cast<const unsigned *>(vr));
+        const float2 v0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
+        vf[0] = v0.x; vf[1] = v0.y;
+      }
+#pragma unroll
+      for (int h = 0; h < MAX_GROUP; ++h)
+        if (h < G) {
+          const float pj = ps[h * ATT_SUB + jj];
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj, vf[e], acc[h][e]);
+        }
+    }
+    consumer_sync();
+  }
+
+  // cross-warp sum of the partial outputs, then publish (m, l, o) of this piece
+#pragma unroll
+  for (int h = 0; h < MAX_GROUP; ++h)
+    if (h < G)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) red[((size_t)warp * G + h) * DH + lane * DPL + e] = acc[h][e];
+  consumer_sync();
+  const size_t piece = (size_t)g * p.smax + sp;
+  for (int i = tid; i < G * DH; i += NCT) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NCW; ++w) t += red[(size_t)w * G * DH + i];
+    p.part_o[piece * G * DH + i] = t;
+  }
+  if (tid < G) {
+    p.part_ml[(piece * G + tid) * 2] = mrun[tid];
+    p.part_ml[(piece * G + tid) * 2 + 1] = lrun[tid];
+  }
+  consumer_sync();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(&p.ctl->att_cnt[g], 1u);
+    const int last = old == (unsigned)(S - 1);
+    if (last) {
+      p.ctl->att_cnt[g] = 0u;  // next use is a later layer, after several grid barriers
+      __threadfence();
+    }
+    s.flags[1] = last;
+  }
+  consumer_sync();
+  if (s.flags[1]) {
+    for (int i = tid; i < G * DH; i += NCT) {
+      const int h = i / DH;
+      float M = -INFINITY;
+      for (int q = 0; q < S; ++q) M = fmaxf(M, __ldcg(p.part_ml + (((size_t)g * p.smax + q) * G + h) * 2));
+      float num = 0.f, den = 0.f;
+      for (int q = 0; q < S; ++q) {
+        const size_t pc = (size_t)g * p.smax + q;
+        const float w = expf(__ldcg(p.part_ml + (pc * G + h) * 2) - M);
+        den = fmaf(w, __ldcg(p.part_ml + (pc * G + h) * 2 + 1), den);
+        num = fmaf(w, __ldcg(p.part_o + pc * G * DH + i), num);
+      }
+      p.o[(size_t)g * G * DH + i] = num / den;
+    }
+  }
+}
+
+// ---- the kernel -------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ int split_pieces(const DecodeParams &p, int c) {
+  const int by_len = (c + ATT_MIN_CHUNK - 1) / ATT_MIN_CHUNK;
+  return by_len < p.smax ? by_len : p.smax;
+}
+
+__device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard &g) {
+  const uint64_t policy = l2_evict_first_policy();
+  RingPos rp{0, 0u, 0};
+  const RowRange rq = rows_of_cta((p.Hq + 2 * p.Hkv) * p.dh, p.n_cta, blockIdx.x);
+  const RowRange ro = rows_of_cta(p.d, p.n_cta, blockIdx.x);
+  const RowRange rg = rows_of_cta(2 * p.F, p.n_cta, blockIdx.x);
+  const RowRange rl = rows_of_cta(p.V, p.n_cta, blockIdx.x);
+  const int dq = p.Hq * p.dh;
+  bool ok = true;
+  for (int t = 0; t < p.n && ok; ++t) {
+    for (int l = 0; l < p.L && ok; ++l) {
+      const uint8_t *lw = p.wbase + (size_t)l * p.layer_stride;
+      ok = ok && produce_region(lw + p.off_qkv + (size_t)rq.r0 * p.d * 2, rq.r1 - rq.r0, p.d, s, p.nslot, rp, policy, g);
+      ok = ok && produce_region(lw + p.off_wo + (size_t)ro.r0 * dq * 2, ro.r1 - ro.r0, dq, s, p.nslot, rp, policy, g);
+      ok = ok && produce_region(lw + p.off_gu + (size_t)rg.r0 * p.d * 2, rg.r1 - rg.r0, p.d, s, p.nslot, rp, policy, g);
+      ok = ok && produce_region(lw + p.off_down + (size_t)ro.r0 * p.F * 2, ro.r1 - ro.r0, p.F, s, p.nslot, rp, policy, g);
+    }
+    if (ok && (!p.lm_last_only || t == p.n - 1))
+      ok = produce_region(p.w_lm + (size_t)rl.r0 * p.d * 2, rl.r1 - rl.r0, p.d, s, p.nslot, rp, policy, g);
+  }
+  drain_ring(s, p.nslot, rp, g);
+}
+
+__device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard &g) {
+  const int tid = threadIdx.x;
+  const RowRange rq = rows_of_cta((p.Hq + 2 * p.Hkv) * p.dh, p.n_cta, blockIdx.x);
+  const RowRange ro = rows_of_cta(p.d, p.n_cta, blockIdx.x);
+  const RowRange rg = rows_of_cta(2 * p.F, p.n_cta, blockIdx.x);
+  const RowRange rl = rows_of_cta(p.V, p.n_cta, blockIdx.x);
+  const int dq = p.Hq * p.dh;
+  RingPos rp{0, 0u, 0};
+  uint32_t gen = 0;
+  unsigned long long wait_ns = 0;
+  bool ok = true;
+  const uint64_t t_start = globaltimer();
+
+  for (int t = 0; t < p.n && ok; ++t) {
+    const int pos = p.pos0 + t;
+    // the token this step consumes, and the token greedy decode emits here
+    const int predicted = t == 0 ? p.persist->next_token : key_index(__ldcg(&p.ctl->amax[(t - 1) & 1]));
+    int token = p.mode == MODE_FORCED ? p.forced[t] : predicted;
+    token = token < 0 ? 0 : (token >= p.V ? p.V - 1 : token);  // ids are checked on the host; never read outside E
+    if (blockIdx.x == 0 && tid == 0 && p.out_tokens) p.out_tokens[t] = predicted;
+
+    // embed: stage E[token], keep this CTA's residual slice in x
+    float ss = stage_f16(s, p.embed + (size_t)token * p.d, p.d, true);
+    for (int i = ro.r0 + tid; i < ro.r1; i += NCT) p.x[i] = s.vec[i];
+
+    for (int l = 0; l < p.L; ++l) {
+      // [QKV] + RoPE + K/V append
+      if (l > 0) ss = stage_f32(s, p.x, p.d, true);
+      consume_region(s, p.nslot, rp, rq.r1 - rq.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
+      consumer_sync();
+      epilogue_qkv(p, s, l, pos, rq.r0, rq.r1);
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+      if (l == 0 && blockIdx.x == 0 && tid == 0) p.ctl->amax[(t + 1) & 1] = 0ull;  // every CTA has read it
+
+      // [ATT] split-KV attention over c = pos + 1 positions
+      {
+        const int c = pos + 1;
+        const int S = split_pieces(p, c);
+        const int C = (c + S - 1) / S;
+        const int item = blockIdx.x;
+        if (item < p.Hkv * S) {
+          const int gk = item / S, sp = item % S;
+          const int j0 = min(c, sp * C), j1 = min(c, j0 + C);
+          if (p.dh == 128)
+            attention_piece<4>(p, s, l, gk, sp, S, j0, j1);
+          else
+            attention_piece<2>(p, s, l, gk, sp, S, j0, j1);
+        }
+      }
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+
+      // [WO] h = x + Wo o
+      stage_f32(s, p.o, dq, false);
+      consume_region(s, p.nslot, rp, ro.r1 - ro.r0, dq, 1.0f, g);
+      consumer_sync();
+      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.h[ro.r0 + i] = p.x[ro.r0 + i] + s.out[i];
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+
+      // [GU] a = silu(gate) * up
+      ss = stage_f32(s, p.h, p.d, true);
+      consume_region(s, p.nslot, rp, rg.r1 - rg.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
+      consumer_sync();
+      for (int pr = tid; pr < (rg.r1 - rg.r0) / 2; pr += NCT) {
+        const float gt = s.out[2 * pr], up = s.out[2 * pr + 1];
+        p.a[rg.r0 / 2 + pr] = gt / (1.0f + expf(-gt)) * up;
+      }
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+
+      // [DOWN] x = h + Wd a
+      stage_f32(s, p.a, p.F, false);
+      consume_region(s, p.nslot, rp, ro.r1 - ro.r0, p.F, 1.0f, g);
+      consumer_sync();
+      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.x[ro.r0 + i] = p.h[ro.r0 + i] + s.out[i];
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+    }
+    if (!ok) break;
+
+    // [LM] logits and greedy argmax
+    if (!p.lm_last_only || t == p.n - 1) {
+      ss = stage_f32(s, p.x, p.d, true);
+      consume_region(s, p.nslot, rp, rl.r1 - rl.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
+      consumer_sync();
+      float *dst = p.out_logits ? p.out_logits + (size_t)t * p.V : nullptr;
+      unsigned long long best = 0ull;
+      for (int i = tid; i < rl.r1 - rl.r0; i += NCT) {
+        const float v = s.out[i];
+        p.logits[rl.r0 + i] = v;
+        if (dst) dst[rl.r0 + i] = v;
+        const unsigned long long k = argmax_key(v, rl.r0 + i);
+        best = k > best ? k : best;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if ((tid & 31) == 0) s.kred[tid >> 5] = best;
+      consumer_sync();
+      if (tid == 0) {
+        unsigned long long b = 0ull;
+        for (int w = 0; w < NCW; ++w) b = s.kred[w] > b ? s.kred[w] : b;
+        if (b) atomicMax(&p.ctl->amax[t & 1], b);
+      }
+      if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+      if (t == p.n - 1 && blockIdx.x == 0 && tid == 0)
+        p.persist->next_token = key_index(__ldcg(&p.ctl->amax[t & 1]));
+    }
+  }
+  if (tid == 0) {
+    unsigned long long *st = p.cta_stats + (size_t)blockIdx.x * 4;
+    st[0] = wait_ns;
+    st[1] = gen;
+    st[2] = t_start;
+    st[3] = globaltimer();
+  }
+}
+
+__global__ void __launch_bounds__(BLOCK, 1) decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem s = carve_smem(smem_raw, p.nslot, p.vec_floats, p.out_floats);
+  init_ring(s, p.nslot);
+  const Guard g{&p.ctl->status, p.timeout_ns};
+  if (threadIdx.x >= NCT) {
+    if (threadIdx.x == NCT) producer_main(p, s, g);
+    return;
+  }
+  consumer_main(p, s, g);
+}
+
+}  // namespace kie
+
+// Launch helper used by the C ABI (kie_api.cu).
+cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(kie::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void *args[] = {(void *)&p};
+  return cudaLaunchCooperativeKernel((const void *)kie::decode_kernel, dim3(p.n_cta), dim3(kie::BLOCK), args, smem,
+                                     stream);
+}
+
+int kie_decode_max_blocks_per_sm(size_t smem) {
+  int nb = 0;
+  cudaFuncSetAttribute(kie::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kie::decode_kernel, kie::BLOCK, smem) != cudaSuccess) return -1;
+  return nb;
+}

@@ -1,0 +1,62 @@
+// Parameters and control block of the persistent decode kernel (shared by the kernel and the C ABI).
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kie {
+
+constexpr int MAX_GROUP = 8;         // query heads per KV head supported by the attention step
+constexpr int ATT_SUB = 64;          // positions per online-softmax sub-chunk
+constexpr int ATT_MIN_CHUNK = 32;    // fewest positions a split-KV CTA takes
+constexpr int MAX_KV_HEADS = 64;
+constexpr int TRACE_CAP = 4096;      // grid barriers whose per-CTA waits are recorded per launch
+
+// Zeroed by the host before every launch.
+struct Ctl {
+  unsigned bar_count;
+  unsigned pad0[31];
+  int status;
+  int where;
+  unsigned pad1[30];
+  unsigned long long amax[2];  // packed (orderable logit, ~index) argmax of the even / odd token
+  unsigned pad2[28];
+  unsigned att_cnt[MAX_KV_HEADS];  // split-KV arrivals per KV head; the last arrival merges and resets
+};
+
+// Survives across launches.
+struct Persist {
+  int next_token;  // argmax of the current logits
+  int pad[31];
+};
+
+enum Mode { MODE_DECODE = 0, MODE_FORCED = 1 };
+
+struct DecodeParams {
+  int L, d, Hq, Hkv, dh, F, V, max_seq;
+  int n_cta, nslot, vec_floats, out_floats;
+  float eps;
+  // packed weights: layer l's projections start at wbase + l * layer_stride (+ off_*)
+  const uint8_t *wbase;
+  long long layer_stride, off_qkv, off_wo, off_gu, off_down;
+  const uint8_t *w_lm;
+  const __half *embed;  // [V][d], plain
+  // state and activations (device)
+  __half *kv;           // [L][2][Hkv][max_seq][dh]; K rows hold each RoPE pair (i, i + dh/2) adjacent
+  const float2 *rope;   // [max_seq][dh/2] (cos, sin)
+  float *x, *h, *q, *o, *a, *logits;
+  float *part_o, *part_ml;  // [Hkv][smax][group][dh], [Hkv][smax][group][2]
+  int smax;                 // split-KV pieces per KV head at most
+  Ctl *ctl;
+  Persist *persist;
+  uint32_t *trace;                 // [TRACE_CAP][n_cta] barrier wait (ns)
+  unsigned long long *cta_stats;   // [n_cta][4]: wait ns, barriers, start, end
+  // this launch
+  int pos0, n, mode, lm_last_only;
+  const int *forced;   // [n] device (forced mode)
+  int *out_tokens;     // [n] device or null
+  float *out_logits;   // [n][V] device or null
+  unsigned long long timeout_ns;
+  int skip_cta, skip_barrier;
+};
+
+}  // namespace kie

@@ -1,0 +1,377 @@
+// Device building blocks shared by the persistent decode kernel and the standalone GEMV kernel.
+//
+// Every CTA runs NCW consumer warps and one producer warp. The producer's elected lane walks the CTA's
+// static sequence of weight tiles (it does not depend on any activation) and moves each tile from HBM
+// into a shared-memory ring slot with one 1-D bulk copy (cp.async.bulk, completion counted on the slot's
+// "full" mbarrier, L2 evict-first policy). Consumers wait on "full", run their part of the dot products
+// from shared memory, and release the slot on its "empty" mbarrier. Because the producer never waits for
+// a grid barrier, weight loads stay in flight while the consumers synchronise with the rest of the grid:
+// the in-kernel weight prefetch of the monokernel pages ("inside the monokernel": FFN weights are
+// prefetched while attention runs), done here by the GB300's bulk-copy engine.
+#pragma once
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "kie_layout.h"
+
+namespace kie {
+
+constexpr int NCW = 8;                          // consumer warps
+constexpr int NCT = NCW * 32;                   // consumer threads
+constexpr int BLOCK = NCT + 32;                 // + one producer warp
+constexpr int ROWS_PER_WARP = TILE_ROWS / NCW;  // rows of a tile each consumer warp owns
+static_assert(TILE_ROWS % NCW == 0, "tile rows must split evenly over consumer warps");
+
+constexpr int ST_OK = 0;
+constexpr int ST_TIMEOUT = 1;
+
+// ---- PTX wrappers --------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// One contiguous global -> shared bulk copy; bytes and both addresses are multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Named barrier 1: the NCT consumer threads of this CTA (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---- shared memory ---------------------------------------------------------------------------------------
+
+struct Smem {
+  uint8_t *ring;           // nslot * SLOT_BYTES
+  float *vec;              // the phase's input vector (fp32), also attention scratch
+  float *out;              // per-CTA row results of the current projection
+  uint64_t *full, *empty;  // ring mbarriers
+  float *red;              // NCW floats of cross-warp reduction scratch
+  unsigned long long *kred;  // NCW keys of cross-warp argmax scratch
+  volatile int *flags;     // [0] abort, [1] last-arriver flag
+  float *scal;             // [0] inv_rms
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Byte size of the dynamic shared memory for a ring of nslot slots, vec_floats input-vector floats and
+// out_floats row results.
+__host__ __device__ inline size_t smem_bytes(int nslot, int vec_floats, int out_floats) {
+  size_t o = (size_t)nslot * SLOT_BYTES;
+  o += align_up((size_t)vec_floats * 4, 128);
+  o += align_up((size_t)out_floats * 4, 128);
+  o += 2 * (size_t)nslot * 8;
+  o += NCW * 4 + NCW * 8 + 16 + 16;
+  return align_up(o, 128);
+}
+
+__device__ inline Smem carve_smem(uint8_t *base, int nslot, int vec_floats, int out_floats) {
+  Smem s;
+  size_t o = 0;
+  s.ring = base;
+  o += (size_t)nslot * SLOT_BYTES;
+  s.vec = (float *)(base + o);
+  o += align_up((size_t)vec_floats * 4, 128);
+  s.out = (float *)(base + o);
+  o += align_up((size_t)out_floats * 4, 128);
+  s.full = (uint64_t *)(base + o);
+  o += (size_t)nslot * 8;
+  s.empty = (uint64_t *)(base + o);
+  o += (size_t)nslot * 8;
+  s.kred = (unsigned long long *)(base + o);
+  o += NCW * 8;
+  s.red = (float *)(base + o);
+  o += NCW * 4;
+  s.flags = (volatile int *)(base + o);
+  o += 16;
+  s.scal = (float *)(base + o);
+  return s;
+}
+
+// Thread 0 initialises the ring barriers; every thread of the block (producer warp included) must call.
+__device__ inline void init_ring(Smem &s, int nslot) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nslot; ++i) {
+      mbar_init(&s.full[i], 1);      // the producer's arrive.expect_tx (+ the copy's bytes)
+      mbar_init(&s.empty[i], NCW);   // one arrival per consumer warp
+    }
+    s.flags[0] = 0;
+    s.flags[1] = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+}
+
+// ---- bounded waits ---------------------------------------------------------------------------------------
+
+// Everything a wait needs to give up cleanly: the launch-wide status word (any CTA may set it) and the
+// wait limit.
+struct Guard {
+  int *status;
+  unsigned long long timeout_ns;
+};
+
+__device__ inline void raise_status(const Guard &g, int code) { atomicCAS(g.status, ST_OK, code); }
+
+// Wait for phase `parity` of an mbarrier. Gives up (returns false) when another CTA has raised the status
+// word or when the wait exceeds the limit, in which case it raises ST_TIMEOUT itself.
+__device__ inline bool wait_mbar(uint64_t *bar, uint32_t parity, const Guard &g) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (int spins = 1;; ++spins) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((spins & 63) == 0) {
+      if (ld_relaxed_gpu(g.status) != ST_OK) return false;
+      if (globaltimer() - t0 > g.timeout_ns) {
+        raise_status(g, ST_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// ---- ring ------------------------------------------------------------------------------------------------
+
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  long long issued;  // producer only: tiles issued so far
+};
+
+__device__ __forceinline__ void ring_advance(RingPos &r, int nslot) {
+  if (++r.slot == nslot) {
+    r.slot = 0;
+    r.phase ^= 1u;
+  }
+}
+
+// Producer: stream the tiles of rows [0, R) of one CTA region (R rows of K columns, packed) into the ring.
+// Returns false if it had to give up (status raised).
+__device__ inline bool produce_region(const uint8_t *region, int R, int K, Smem &s, int nslot, RingPos &rp,
+                                      uint64_t policy, const Guard &g) {
+  const uint8_t *src = region;
+  for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
+    const int rows = min(TILE_ROWS, R - g0);
+    for (int k0 = 0; k0 < K; k0 += TILE_COLS) {
+      const uint32_t bytes = (uint32_t)rows * (uint32_t)min(TILE_COLS, K - k0) * 2u;
+      if (!wait_mbar(&s.empty[rp.slot], rp.phase ^ 1u, g)) return false;
+      mbar_arrive_expect_tx(&s.full[rp.slot], bytes);
+      bulk_g2s(s.ring + (size_t)rp.slot * SLOT_BYTES, src, bytes, &s.full[rp.slot], policy);
+      src += bytes;
+      ++rp.issued;
+      ring_advance(rp, nslot);
+    }
+  }
+  return true;
+}
+
+// Producer, before the CTA may exit: wait until every bulk copy it issued has landed (bounded), so no copy
+// writes into the shared memory of a finished CTA.
+__device__ inline void drain_ring(Smem &s, int nslot, const RingPos &rp, const Guard &g) {
+  Guard local = g;
+  for (int i = 0; i < nslot; ++i) {
+    const long long uses = rp.issued > i ? (rp.issued - i + nslot - 1) / nslot : 0;
+    if (uses == 0) continue;
+    const uint32_t parity = (uint32_t)((uses - 1) & 1);
+    // A landed copy completes its phase whether or not a consumer read it; the limit only guards a fault.
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&s.full[i], parity))
+      if (globaltimer() - t0 > local.timeout_ns) {
+        raise_status(local, ST_TIMEOUT);
+        break;
+      }
+  }
+}
+
+// ---- consumer: one projection over the CTA's rows ------------------------------------------------------
+
+__device__ __forceinline__ float dot8(const uint4 w, const float4 xa, const float4 xb) {
+  const float2 w0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+  const float2 w1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+  const float2 w2 = __half22float2(*reinterpret_cast<const __half2 *>(&w.z));
+  const float2 w3 = __half22float2(*reinterpret_cast<const __half2 *>(&w.w));
+  float a = w0.x * xa.x;
+  a = fmaf(w0.y, xa.y, a);
+  a = fmaf(w1.x, xa.z, a);
+  a = fmaf(w1.y, xa.w, a);
+  float b = w2.x * xb.x;
+  b = fmaf(w2.y, xb.y, b);
+  b = fmaf(w3.x, xb.z, b);
+  b = fmaf(w3.y, xb.w, b);
+  return a + b;
+}
+
+// out[i] = scale * sum_k W[r0 + i][k] * vec[k] for the R rows of this CTA, consuming the tiles the
+// producer streams for this region. A thread whose wait gives up raises the CTA abort flag and skips the
+// remaining waits, but walks the same tile sequence, so every consumer thread still reaches the same
+// named barriers; callers test the flag only after a consumer_sync, where it is CTA-uniform.
+__device__ inline void consume_region(Smem &s, int nslot, RingPos &rp, int R, int K, float scale,
+                                      const Guard &g) {
+  bool ok = s.flags[0] == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float *vec = s.vec;
+  for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
+    const int rows = min(TILE_ROWS, R - g0);
+    float acc[ROWS_PER_WARP];
+#pragma unroll
+    for (int j = 0; j < ROWS_PER_WARP; ++j) acc[j] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += TILE_COLS) {
+      const int w = min(TILE_COLS, K - k0);
+      if (ok && !wait_mbar(&s.full[rp.slot], rp.phase, g)) {
+        ok = false;
+        s.flags[0] = 1;
+      }
+      if (ok && lane * 8 < w) {
+        const uint8_t *tile = s.ring + (size_t)rp.slot * SLOT_BYTES;
+        const float4 xa = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8);
+        const float4 xb = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8 + 4);
+#pragma unroll
+        for (int j = 0; j < ROWS_PER_WARP; ++j) {
+          const int r = warp + NCW * j;
+          if (r < rows) {
+            const uint4 wv = *reinterpret_cast<const uint4 *>(tile + ((size_t)r * w + lane * 8) * 2);
+            acc[j] += dot8(wv, xa, xb);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.empty[rp.slot]);
+      ring_advance(rp, nslot);
+    }
+#pragma unroll
+    for (int j = 0; j < ROWS_PER_WARP; ++j) {
+      const int r = warp + NCW * j;
+      if (r < rows) {
+        const float v = warp_sum(acc[j]);
+        if (lane == 0) s.out[g0 + r] = v * scale;
+      }
+    }
+  }
+}
+
+// ---- staging the input vector ---------------------------------------------------------------------------
+
+// vec[0..K) = src (fp32, written by other CTAs earlier in the launch: read through L2). If want_ss, returns
+// the CTA-uniform sum of squares (ends with a consumer_sync either way).
+__device__ inline float stage_f32(Smem &s, const float *src, int K, bool want_ss) {
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  for (int i = tid * 4; i < K; i += NCT * 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+    *reinterpret_cast<float4 *>(s.vec + i) = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  if (!want_ss) {
+    consumer_sync();
+    return 0.f;
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) s.red[tid >> 5] = ss;
+  consumer_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) t += s.red[w];
+  consumer_sync();  // s.red may be reused right after
+  return t;
+}
+
+// vec[0..K) = fp32(src) for an fp16 vector that is read-only during the launch.
+__device__ inline float stage_f16(Smem &s, const __half *src, int K, bool want_ss) {
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  for (int i = tid * 8; i < K; i += NCT * 8) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(src + i));
+    const __half2 *h = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(h[e]);
+      s.vec[i + 2 * e] = f.x;
+      s.vec[i + 2 * e + 1] = f.y;
+      ss += f.x * f.x + f.y * f.y;
+    }
+  }
+  if (!want_ss) {
+    consumer_sync();
+    return 0.f;
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) s.red[tid >> 5] = ss;
+  consumer_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) t += s.red[w];
+  consumer_sync();
+  return t;
+}
+
+}  // namespace kie

@@ -1,0 +1,94 @@
+"""Host side of the C ABI, no GPU: the library loads and exports every declared entry point, the per-CTA
+tile layout is a bijection with contiguous tiles, buffer planning and configuration checks behave."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import persistent_monokernel_decode_gb300 as kie
+from synth.configs import TINY, TWO_B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    kie.build()
+    yield
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "kie.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kie_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    names = declared_entry_points()
+    assert len(names) >= 20
+    L = kie.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in kie.SIGNATURES, f"{n} has no ctypes signature in the binding"
+    assert set(kie.SIGNATURES) == set(names)
+
+
+@pytest.mark.parametrize("M,K,n", [(2, 8, 1), (2, 8, 152), (34, 264, 3), (768, 256, 152), (1408, 704, 152),
+                                   (100, 520, 7), (64, 2560, 5)])
+def test_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
+    off = np.array([[kie.packed_offset(M, K, n, r, c) for c in range(K)] for r in range(M)], dtype=np.int64)
+    assert np.array_equal(np.sort(off.ravel()), np.arange(M * K))
+    for cta in range(n):
+        r0, r1 = kie.rows_of_cta(M, n, cta)
+        if r1 == r0:
+            continue
+        block = off[r0:r1]
+        assert block.min() == r0 * K and block.max() == r1 * K - 1  # the CTA's region is contiguous
+        for g0 in range(0, r1 - r0, 32):
+            rows = min(32, r1 - r0 - g0)
+            for k0 in range(0, K, 256):
+                w = min(256, K - k0)
+                tile = block[g0:g0 + rows, k0:k0 + w]
+                # one row-major run of rows*w elements
+                assert np.array_equal(tile.ravel() - tile.min(), np.arange(rows * w))
+
+
+@pytest.mark.parametrize("M,n", [(2, 1), (2, 152), (256, 152), (3584, 152), (15360, 152), (32000, 152), (10, 3)])
+def test_row_split_pairs_cover_and_balance(M, n):
+    spans = [kie.rows_of_cta(M, n, i) for i in range(n)]
+    assert spans[0][0] == 0 and spans[-1][1] == M
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 == b0
+    sizes = [r1 - r0 for r0, r1 in spans]
+    assert all(s % 2 == 0 for s in sizes)
+    assert max(sizes) - min(sizes) <= 2
+
+
+def test_buffer_plan_without_a_device():
+    cfg = kie.make_config(TWO_B, 1152)
+    s = kie.kie_query_buffers(cfg, 152)
+    assert s.n_cta == 152
+    assert s.weights_bytes >= TWO_B.weight_bytes_per_token() + TWO_B.vocab * TWO_B.d_model * 2
+    assert s.kv_bytes >= TWO_B.kv_bytes_per_token(1152)
+    assert s.workspace_bytes < 64 << 20
+    t = kie.kie_query_buffers(kie.make_config(TINY, 48), 152)
+    assert t.weights_bytes >= TINY.weight_bytes_per_token()
+
+
+@pytest.mark.parametrize("field,value", [("head_dim", 96), ("n_kv_heads", 3), ("vocab", 4095), ("d_model", 260),
+                                         ("n_layers", 0), ("ffn_dim", 700), ("max_seq", 0)])
+def test_unsupported_configs_are_rejected(field, value):
+    cfg = kie.make_config(TINY, 64)
+    setattr(cfg, field, value)
+    with pytest.raises(kie.KieError) as e:
+        kie.kie_query_buffers(cfg, 152)
+    assert e.value.code == kie.KIE_ERR_INVALID
+
+
+def test_product_path_fails_loudly_without_a_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(RuntimeError):
+        kie.Decoder(TINY, {}, 16)

@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Tolerances (the acceptance bar of this port): GEMV relative error <= 1e-3 against fp64; logits max |diff|
+<= 2e-2 at every step; greedy tokens identical wherever the oracle's top-1/top-2 margin exceeds 2e-2, with
+teacher forcing (the oracle's tokens fed to both sides) so one permitted divergence cannot cascade.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.configs import GEMV_SHAPES, TINY, TINY_DECODE, TWO_B, ModelConfig
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL = 2e-2
+MARGIN = 2e-2
+
+
+@pytest.fixture(scope="module")
+def kie():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import persistent_monokernel_decode_gb300 as k
+    k.build()
+    return k
+
+
+def margins(logits):
+    s = np.sort(logits, axis=-1)
+    return s[..., -1] - s[..., -2]
+
+
+def check_run(dec, cfg, w, prompt, n, max_seq):
+    """Prefill + teacher-forced decode against the oracle; returns the max logit error seen."""
+    ref_tokens, ref_logits = oracle.generate(cfg, w, prompt, n, max_seq=max_seq)
+    dec.reset()
+    dec.prefill(prompt)
+    err = float(np.max(np.abs(dec.logits() - ref_logits[0])))
+    assert err <= LOGIT_TOL, f"prefill logits differ by {err}"
+    toks, logits = dec.decode_forced(ref_tokens)
+    diff = np.max(np.abs(logits - ref_logits[1:]), axis=1)
+    assert diff.max() <= LOGIT_TOL, f"step {int(diff.argmax())}: logits differ by {diff.max()}"
+    sure = margins(ref_logits[:-1]) > MARGIN
+    assert np.array_equal(toks[sure], ref_tokens[sure])
+    return max(err, float(diff.max())), ref_tokens, ref_logits
+
+
+# ---- GEMV -----------------------------------------------------------------------------------------------
+
+def gemv_check(kie, W, x, n_cta=0):
+    import torch
+    M, K = W.shape
+    Wd = torch.from_numpy(W.view(np.int16)).cuda()
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    packed = kie.gemv_pack(Wd, n_cta)
+    y = kie.gemv(packed, xd, M, K, n_cta).cpu().numpy()
+    torch.cuda.synchronize()
+    y64 = oracle.gemv(W, synth.as_f32(x).astype(np.float64), 64)
+    rel = np.max(np.abs(y - y64)) / max(np.max(np.abs(y64)), 1e-30)
+    assert rel <= 1e-3, (M, K, rel)
+    absdot = oracle.gemv(W & 0x7FFF, np.abs(synth.as_f32(x)).astype(np.float64), 64)
+    assert np.all(np.abs(y - y64) <= 1e-3 * absdot + 1e-6)
+    return rel
+
+
+@pytest.mark.parametrize("M,K,n_cta", [(2, 8, 0), (2, 8, 1), (34, 264, 3), (1000, 2056, 0), (66, 520, 5),
+                                       (4096, 704, 0), (32000, 256, 0)])
+def test_gemv_small_and_ragged(kie, M, K, n_cta):
+    W = synth.normal_f16(11, M + K, (M, K), 0.0, 1.0 / np.sqrt(K))
+    x = synth.normal_f16(11, 7, K, 0.0, 1.0)
+    gemv_check(kie, W, x, n_cta)
+
+
+@pytest.mark.parametrize("shape", GEMV_SHAPES, ids=lambda s: f"{s.M}x{s.K}")
+def test_gemv_sweep_shapes(kie, shape):
+    W, x = synth.gemv_operands(shape)
+    gemv_check(kie, W, x)
+
+
+# ---- tiny decoder ---------------------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def tiny(kie):
+    w = synth.model_weights(TINY)
+    wl = TINY_DECODE
+    dec = kie.Decoder(TINY, w, max_seq=wl.prompt_len + wl.decode_len)
+    yield w, dec
+    dec.close()
+
+
+def test_tiny_teacher_forced_parity(tiny):
+    w, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    check_run(dec, TINY, w, prompt, TINY_DECODE.decode_len, TINY_DECODE.prompt_len + TINY_DECODE.decode_len)
+
+
+def test_tiny_free_running_greedy_matches_until_a_close_call(tiny):
+    w, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    n = TINY_DECODE.decode_len
+    ref_tokens, ref_logits = oracle.generate(TINY, w, prompt, n)
+    dec.reset()
+    dec.prefill(prompt)
+    toks = dec.decode(n)
+    m = margins(ref_logits[:-1])
+    first_close = int(np.argmax(m <= MARGIN)) if np.any(m <= MARGIN) else n
+    assert np.array_equal(toks[:first_close], ref_tokens[:first_close])
+    assert dec.position == len(prompt) + n
+
+
+def test_split_calls_equal_one_call(tiny):
+    _, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    whole = dec.decode(20)
+    dec.reset()
+    dec.prefill(prompt[:5])
+    dec.prefill(prompt[5:])
+    parts = np.concatenate([dec.decode(7), dec.decode(1), dec.decode(12)])
+    assert np.array_equal(whole, parts)
+
+
+def test_prefill_in_pieces_equals_whole(tiny):
+    _, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    a = dec.logits()
+    dec.reset()
+    for i in range(0, len(prompt), 3):
+        dec.prefill(prompt[i:i + 3])
+    np.testing.assert_array_equal(dec.logits(), a)
+
+
+def test_api_errors(tiny, kie):
+    _, dec = tiny
+    dec.reset()
+    with pytest.raises(kie.KieError) as e:
+        dec.decode(1)
+    assert e.value.code == kie.KIE_ERR_INVALID
+    with pytest.raises(kie.KieError) as e:
+        dec.prefill([TINY.vocab])
+    assert e.value.code == kie.KIE_ERR_INVALID
+    dec.prefill([1, 2, 3])
+    with pytest.raises(kie.KieError) as e:
+        dec.decode(dec.max_seq)
+    assert e.value.code == kie.KIE_ERR_CAPACITY
+    assert dec.position == 3
+
+
+def test_barrier_stats(tiny):
+    _, dec = tiny
+    dec.reset()
+    dec.prefill(synth.prompt(TINY_DECODE))
+    dec.decode(4)
+    st = dec.barrier_stats()
+    assert st["barriers"] == 4 * (5 * TINY.n_layers + 1)
+    assert 0 < st["mean_latency_ns"] <= st["mean_wait_ns"] + 1e-9
+    assert st["total_ns"] > 0
+
+
+def test_wait_limit_ends_a_stuck_launch_cleanly(tiny, kie):
+    """One CTA skips one grid-barrier arrival: every other CTA's bounded wait runs out, the launch returns
+    KIE_ERR_TIMEOUT, and the context is usable again afterwards."""
+    w, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    dec.set_timeout_ns(20_000_000)
+    dec.debug_skip_arrival(cta=3, barrier=2)
+    with pytest.raises(kie.KieError) as e:
+        dec.decode(4)
+    assert e.value.code == kie.KIE_ERR_TIMEOUT
+    dec.set_timeout_ns(1_000_000_000)
+    check_run(dec, TINY, w, prompt, 8, dec.max_seq)
+
+
+# ---- structure variants ---------------------------------------------------------------------------------
+
+VARIANTS = {
+    # GQA 4:1 with dh = 128 and a non-multiple-of-256 width, gains != 1 (folding exercised)
+    "gqa_dh128": ModelConfig("v1", n_layers=3, d_model=384, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=1000,
+                             vocab=1000, seed=5, gain_std=0.1),
+    # the largest group the attention step supports (8 query heads per KV head), dh = 64
+    "group8_dh64": ModelConfig("v2", n_layers=2, d_model=512, n_heads=8, n_kv_heads=1, head_dim=64, ffn_dim=1376,
+                               vocab=2050, seed=6, gain_std=0.05),
+}
+
+
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+def test_structure_variants(kie, name):
+    cfg = VARIANTS[name]
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(cfg.seed, 40, cfg.vocab)
+    dec = kie.Decoder(cfg, w, max_seq=64)
+    check_run(dec, cfg, w, prompt, 20, 64)
+    dec.close()
+
+
+def test_long_context_split_kv(kie):
+    """Tiny model at 1,500 positions: split-KV with the maximum number of pieces, long chunks, several
+    online-softmax sub-chunks per piece."""
+    cfg = dataclasses.replace(TINY, seed=9)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(9, 1500, cfg.vocab)
+    dec = kie.Decoder(cfg, w, max_seq=1516)
+    check_run(dec, cfg, w, prompt, 12, 1516)
+    dec.close()
+
+
+# ---- the 2B workload at full size, in the launch configuration the bench times ---------------------------
+
+@pytest.fixture(scope="module")
+def two_b(kie):
+    w = synth.model_weights(TWO_B)
+    dec = kie.Decoder(TWO_B, w, max_seq=128 + 1024)
+    yield w, dec
+    dec.close()
+
+
+def test_2b_sampled_steps_match_oracle(two_b):
+    """Prompt of 128 ids and the first 8 teacher-forced decode steps of the 2B model, against the oracle."""
+    w, dec = two_b
+    prompt = synth.tokens(TWO_B.seed, 128, TWO_B.vocab)
+    check_run(dec, TWO_B, w, prompt, 8, 128 + 1024)
+
+
+def test_2b_full_decode_properties(two_b):
+    """All 1,024 greedy tokens of the bench workload: valid ids, position bookkeeping, and identical tokens
+    when the same decode is split into two calls."""
+    _, dec = two_b
+    prompt = synth.tokens(TWO_B.seed, 128, TWO_B.vocab)
+    dec.reset()
+    dec.prefill(prompt)
+    whole = dec.decode(1024)
+    assert whole.min() >= 0 and whole.max() < TWO_B.vocab
+    assert dec.position == 128 + 1024
+    dec.reset()
+    dec.prefill(prompt)
+    parts = np.concatenate([dec.decode(300), dec.decode(724)])
+    assert np.array_equal(whole, parts)
+    st = dec.barrier_stats()
+    assert st["barriers"] == 724 * (5 * TWO_B.n_layers + 1)
