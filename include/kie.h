@@ -132,6 +132,12 @@ typedef struct {
 } kie_barrier_stats;
 int kie_get_barrier_stats(kie_ctx *ctx, kie_barrier_stats *out);
 
+/* Raw barrier trace of the last launch (the first 4096 grid barriers): for barrier b in
+ * [first, first + count) and CTA i, arrive_ns[(b - first) * n_cta + i] is the %globaltimer value when CTA i
+ * arrived and wait_ns[...] how long it waited. Host arrays of count * n_cta entries. Returns the number of
+ * barriers copied (>= 0) or a negative error code. */
+int kie_get_barrier_trace(kie_ctx *ctx, int first, int count, uint64_t *arrive_ns, uint32_t *wait_ns);
+
 /* Test hook (fault injection on the host side of the contract): if cta >= 0, that CTA skips its arrival
  * at grid barrier number `barrier` of the next launch, so every other CTA's wait runs out and the launch
  * returns KIE_ERR_TIMEOUT after the configured limit. No GPU fault, trap or unbounded wait is involved. */

@@ -112,6 +112,7 @@ SIGNATURES = {
     "kie_reset": ([P], ctypes.c_int),
     "kie_set_timeout_ns": ([P, ctypes.c_uint64], ctypes.c_int),
     "kie_get_barrier_stats": ([P, P], ctypes.c_int),
+    "kie_get_barrier_trace": ([P, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
     "kie_debug_skip_arrival": ([P, ctypes.c_int, ctypes.c_int], ctypes.c_int),
     "kie_n_cta": ([P], ctypes.c_int),
     "kie_last_error": ([P], ctypes.c_char_p),
@@ -269,6 +270,15 @@ class Decoder:
         _check(lib().kie_get_barrier_stats(self.ctx, ctypes.byref(st)), self.ctx)
         return {"barriers": st.barriers, "mean_wait_ns": st.mean_wait_ns,
                 "mean_latency_ns": st.mean_latency_ns, "total_ns": st.total_ns}
+
+    def barrier_trace(self, first: int = 0, count: int = 4096):
+        """(arrive_ns [m, n_cta] uint64, wait_ns [m, n_cta] uint32) for barriers first..first+m-1."""
+        arrive = np.zeros((count, self.n_cta), dtype=np.uint64)
+        wait = np.zeros((count, self.n_cta), dtype=np.uint32)
+        m = lib().kie_get_barrier_trace(self.ctx, first, count, arrive.ctypes.data, wait.ctypes.data)
+        if m < 0:
+            _check(m, self.ctx)
+        return arrive[:m], wait[:m]
 
     def debug_skip_arrival(self, cta: int, barrier: int) -> None:
         _check(lib().kie_debug_skip_arrival(self.ctx, cta, barrier), self.ctx)

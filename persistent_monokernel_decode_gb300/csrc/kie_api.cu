@@ -35,7 +35,8 @@ struct WeightLayout {
 };
 
 struct WsLayout {
-  size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, stats, tok_in, tok_out, chunk, total;
+  size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
+      total;
   int smax;
 };
 
@@ -116,6 +117,7 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   s.ctl = take(sizeof(kie::Ctl));
   s.persist = take(sizeof(kie::Persist));
   s.trace = take((size_t)kie::TRACE_CAP * n_cta * 4);
+  s.trace_arrive = take((size_t)kie::TRACE_CAP * n_cta * 8);
   s.stats = take((size_t)n_cta * 4 * 8);
   s.tok_in = take((size_t)c->max_seq * 4);
   s.tok_out = take((size_t)c->max_seq * 4);
@@ -316,6 +318,7 @@ void fill_base(kie_ctx *ctx) {
   p.ctl = (kie::Ctl *)(ws + pl.ws.ctl);
   p.persist = (kie::Persist *)(ws + pl.ws.persist);
   p.trace = (uint32_t *)(ws + pl.ws.trace);
+  p.trace_arrive = (unsigned long long *)(ws + pl.ws.trace_arrive);
   p.cta_stats = (unsigned long long *)(ws + pl.ws.stats);
   p.skip_cta = -1;
   p.skip_barrier = -1;
@@ -591,6 +594,26 @@ int kie_get_barrier_stats(kie_ctx *ctx, kie_barrier_stats *out) {
   return KIE_OK;
 }
 
+int kie_get_barrier_trace(kie_ctx *ctx, int first, int count, uint64_t *arrive_ns, uint32_t *wait_ns) {
+  if (!ctx || first < 0 || count < 0 || (count > 0 && (!arrive_ns || !wait_ns)))
+    return fail(ctx, KIE_ERR_INVALID, "bad trace request");
+  const Plan &pl = ctx->plan;
+  const size_t n = (size_t)pl.n_cta;
+  unsigned long long bars = 0;
+  KIE_CUDA(ctx, cudaMemcpyAsync(&bars, ctx->wsbuf + pl.ws.stats + 8, 8, cudaMemcpyDeviceToHost, ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  const long long avail = std::min<long long>((long long)bars, kie::TRACE_CAP);
+  const int m = (int)std::max<long long>(0, std::min<long long>(count, avail - first));
+  if (m > 0) {
+    KIE_CUDA(ctx, cudaMemcpyAsync(arrive_ns, ctx->wsbuf + pl.ws.trace_arrive + (size_t)first * n * 8, (size_t)m * n * 8,
+                                  cudaMemcpyDeviceToHost, ctx->stream));
+    KIE_CUDA(ctx, cudaMemcpyAsync(wait_ns, ctx->wsbuf + pl.ws.trace + (size_t)first * n * 4, (size_t)m * n * 4,
+                                  cudaMemcpyDeviceToHost, ctx->stream));
+    KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  }
+  return m;
+}
+
 int kie_debug_skip_arrival(kie_ctx *ctx, int cta, int barrier) {
   if (!ctx) return KIE_ERR_INVALID;
   ctx->skip_cta = cta;
@@ -664,3 +687,4 @@ int kie_rows_of_cta(int M, int n_cta, int cta, int *r0, int *r1) {
 }
 
 }  // extern "C"
+

@@ -59,7 +59,10 @@ __device__ inline bool grid_barrier(const DecodeParams &p, Smem &s, uint32_t &ge
     }
     const uint64_t dt = globaltimer() - t0;
     wait_ns += dt;
-    if (idx < (uint32_t)TRACE_CAP) p.trace[(size_t)idx * p.n_cta + blockIdx.x] = (uint32_t)min(dt, (uint64_t)0xFFFFFFFFu);
+    if (idx < (uint32_t)TRACE_CAP) {
+      p.trace[(size_t)idx * p.n_cta + blockIdx.x] = (uint32_t)min(dt, (uint64_t)0xFFFFFFFFu);
+      p.trace_arrive[(size_t)idx * p.n_cta + blockIdx.x] = t0;
+    }
     if (!ok) s.flags[0] = 1;
   }
   consumer_sync();

@@ -49,6 +49,7 @@ struct DecodeParams {
   Ctl *ctl;
   Persist *persist;
   uint32_t *trace;                 // [TRACE_CAP][n_cta] barrier wait (ns)
+  unsigned long long *trace_arrive;  // [TRACE_CAP][n_cta] %globaltimer at arrival (ns)
   unsigned long long *cta_stats;   // [n_cta][4]: wait ns, barriers, start, end
   // this launch
   int pos0, n, mode, lm_last_only;
