@@ -163,6 +163,25 @@ int kie_gemv_pack(const uint16_t *W_dev, int M, int K, int n_cta, uint16_t *pack
 int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, int M, int K, int n_cta,
              void *stream);
 
+/* ---- decode without device allocation ---------------------------------------------------------------
+ * No counterpart on the monokernel pages: this entry point exists for callers of this library that cannot
+ * call cudaMalloc once they are running -- for example code whose device memory is owned and capped by a
+ * host framework's allocator, or loops that must not hit cudaMalloc/cudaFree because those calls can
+ * synchronise the device and stall other streams.
+ *
+ * kie_decode_noalloc(ctx, n, out_tokens_dev) has the semantics of kie_decode (n greedy tokens, one launch,
+ * state carried in ctx), but allocates nothing: the per-launch scratch (activations, split-KV partials and
+ * the control block) lives in one static device array of KIE_NOALLOC_SCRATCH_BYTES that every GPU loading
+ * the library holds until the process exits. The caller passes the output: out_tokens_dev, n int32 in
+ * DEVICE memory. The call is synchronous (it waits for the ctx stream) and returns KIE_OK, KIE_ERR_TIMEOUT,
+ * or the errors of kie_decode; a model whose scratch exceeds the array is rejected with KIE_ERR_INVALID
+ * (the message gives both sizes). The first call on a device looks up the array's device address (with
+ * that device current), so make that first call before any stream capture. All calls share the one array
+ * and it keeps the last call's contents (the control block is cleared by every call): calls that overlap
+ * on the GPU, from any ctx on the same device, race with each other and must be serialised by the caller. */
+#define KIE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
+int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
+
 /* Host-side layout query (no GPU needed): element offset of W[r][c] inside the packed matrix. */
 int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c);
 

@@ -120,6 +120,7 @@ SIGNATURES = {
     "kie_gemv_packed_bytes": ([ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
     "kie_gemv_pack": ([P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
     "kie_gemv": ([P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P], ctypes.c_int),
+    "kie_decode_noalloc": ([P, ctypes.c_int, P], ctypes.c_int),
     "kie_packed_offset": ([ctypes.c_int] * 5, ctypes.c_int64),
     "kie_rows_of_cta": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
 }
@@ -238,6 +239,10 @@ class Decoder:
     def decode_async(self, n: int, out_dev) -> None:
         """Enqueue n greedy tokens into the device int32 tensor out_dev; no synchronisation."""
         _check(lib().kie_decode_async(self.ctx, n, out_dev.data_ptr()), self.ctx)
+
+    def decode_noalloc(self, n: int, out_dev) -> None:
+        """n greedy tokens into the device int32 tensor out_dev, with no device allocation (static scratch)."""
+        _check(lib().kie_decode_noalloc(self.ctx, n, out_dev.data_ptr()), self.ctx)
 
     def sync(self) -> None:
         _check(lib().kie_sync(self.ctx), self.ctx)

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -688,3 +689,117 @@ int kie_rows_of_cta(int M, int n_cta, int cta, int *r0, int *r1) {
 
 }  // extern "C"
 
+// ---- decode without device allocation ---------------------------------------------------------------------
+//
+// kie_decode_noalloc runs the same kernel as kie_decode, but the per-launch scratch (activations, split-KV
+// partials and the control block) lives in the static array below instead of the ctx workspace. Nothing in
+// this path allocates device or host memory. The array is a file-scope __device__ object, so each GPU that
+// loads the library holds KIE_NOALLOC_SCRATCH_BYTES of it until the process exits; host code never uses its
+// name as an address, only the device address that cudaGetSymbolAddress returns for the current device.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KIE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+void *g_noalloc_addr[NOALLOC_MAX_DEVICES];  // device address of g_noalloc_scratch per device (null: not set up)
+std::mutex g_noalloc_mutex;
+
+struct NoallocLayout {
+  size_t x, h, q, o, a, part_o, part_ml, ctl, total;
+};
+
+NoallocLayout noalloc_layout(const kie_config &c, const Plan &pl) {
+  const int dq = c.n_heads * c.head_dim, G = c.n_heads / c.n_kv_heads;
+  NoallocLayout s;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  s.x = take((size_t)c.d_model * 4);
+  s.h = take((size_t)c.d_model * 4);
+  s.q = take((size_t)dq * 4);
+  s.o = take((size_t)dq * 4);
+  s.a = take((size_t)c.ffn_dim * 4);
+  s.part_o = take((size_t)c.n_kv_heads * pl.ws.smax * G * c.head_dim * 4);
+  s.part_ml = take((size_t)c.n_kv_heads * pl.ws.smax * G * 2 * 4);
+  s.ctl = take(sizeof(kie::Ctl));
+  s.total = o;
+  return s;
+}
+
+// Once per device, with that device current: the device address of the static scratch array.
+int noalloc_scratch(kie_ctx *ctx, uint8_t **out) {
+  int dev = 0;
+  KIE_CUDA(ctx, cudaGetDevice(&dev));
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(ctx, KIE_ERR_INVALID, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(ctx, e, "cudaGetSymbolAddress(static decode scratch)");
+    g_noalloc_addr[dev] = p;
+  }
+  *out = (uint8_t *)g_noalloc_addr[dev];
+  return KIE_OK;
+}
+
+}  // namespace
+
+extern "C" int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (n < 1 || !out_tokens_dev) return fail(ctx, KIE_ERR_INVALID, "decode needs n >= 1 and an output buffer");
+  if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
+  if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
+  const NoallocLayout lay = noalloc_layout(ctx->cfg, ctx->plan);
+  if (lay.total > KIE_NOALLOC_SCRATCH_BYTES) {
+    char buf[200];
+    std::snprintf(buf, sizeof buf,
+                  "this model needs %zu bytes of decode scratch; the static scratch of kie_decode_noalloc holds %u",
+                  lay.total, (unsigned)KIE_NOALLOC_SCRATCH_BYTES);
+    return fail(ctx, KIE_ERR_INVALID, buf);
+  }
+  uint8_t *scr = nullptr;
+  int rc = noalloc_scratch(ctx, &scr);
+  if (rc != KIE_OK) return rc;
+  kie::DecodeParams p = ctx->base;
+  p.x = (float *)(scr + lay.x);
+  p.h = (float *)(scr + lay.h);
+  p.q = (float *)(scr + lay.q);
+  p.o = (float *)(scr + lay.o);
+  p.a = (float *)(scr + lay.a);
+  p.part_o = (float *)(scr + lay.part_o);
+  p.part_ml = (float *)(scr + lay.part_ml);
+  p.ctl = (kie::Ctl *)(scr + lay.ctl);
+  p.pos0 = ctx->pos;
+  p.n = n;
+  p.mode = kie::MODE_DECODE;
+  p.lm_last_only = 0;
+  p.forced = nullptr;
+  p.out_tokens = out_tokens_dev;
+  p.out_logits = nullptr;
+  p.timeout_ns = ctx->timeout_ns;
+  p.skip_cta = p.skip_barrier = -1;
+  // The control block must start at zero; the array keeps whatever the previous call left in it.
+  KIE_CUDA(ctx, cudaMemsetAsync(scr + lay.ctl, 0, sizeof(kie::Ctl), ctx->stream));
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.stats, 0, (size_t)ctx->plan.n_cta * 32, ctx->stream));
+  const cudaError_t e = kie_launch_decode(p, ctx->plan.smem, ctx->stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return fail(ctx, KIE_ERR_LAUNCH, "cooperative launch refused: the grid cannot be co-resident");
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "decode kernel launch");
+  ctx->pos += n;
+  int32_t *st = ctx->pinned + ctx->cfg.max_seq;
+  KIE_CUDA(ctx, cudaMemcpyAsync(st, scr + lay.ctl + offsetof(kie::Ctl, status), 8, cudaMemcpyDeviceToHost,
+                                ctx->stream));
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  if (st[0] != kie::ST_OK) {
+    ctx->pos = 0;
+    ctx->has_logits = false;
+    return fail(ctx, KIE_ERR_TIMEOUT, "device wait timed out; sequence reset");
+  }
+  return KIE_OK;
+}
