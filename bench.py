@@ -159,11 +159,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kie", choices=["kie", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=25, help="fewer layers of the same widths (profiling cases)")
+    ap.add_argument("--prompt", type=int, default=PROMPT)
+    ap.add_argument("--decode", type=int, default=NEW)
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
         return
+
+    import dataclasses
 
     import numpy as np
     import torch
@@ -171,6 +176,11 @@ def main():
     import persistent_monokernel_decode_gb300 as kie
     import synth
     from synth.configs import TWO_B
+
+    model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
+    prompt_len, new = args.prompt, args.decode
+    workload = WORKLOAD if (args.layers, prompt_len, new) == (25, PROMPT, NEW) else \
+        f"llama2b_L{args.layers}_p{prompt_len}_n{new}"
 
     torch.cuda.set_device(local)
     pg = None
@@ -180,11 +190,11 @@ def main():
         pg = dist
     kie.build()
 
-    w = synth.model_weights(TWO_B)
-    prompt = synth.tokens(TWO_B.seed, PROMPT, TWO_B.vocab)
-    dec = kie.Decoder(TWO_B, w, max_seq=PROMPT + NEW)
+    w = synth.model_weights(model)
+    prompt = synth.tokens(model.seed, prompt_len, model.vocab)
+    dec = kie.Decoder(model, w, max_seq=prompt_len + new)
     del w
-    out = torch.empty(NEW, dtype=torch.int32, device="cuda")
+    out = torch.empty(new, dtype=torch.int32, device="cuda")
     stream = dec.stream
 
     def prefill():
@@ -193,7 +203,7 @@ def main():
 
     for _ in range(args.warmup):
         prefill()
-        dec.decode_async(NEW, out)
+        dec.decode_async(new, out)
         dec.sync()
 
     clocks = ClockSampler(local)
@@ -209,7 +219,7 @@ def main():
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        dec.decode_async(NEW, out)
+        dec.decode_async(new, out)
         e1.record(stream)
         dec.sync()
         times.append(e0.elapsed_time(e1) / 1e3)
@@ -221,17 +231,17 @@ def main():
         t = torch.tensor([step_s], device="cuda", dtype=torch.float64)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         step_s = float(t.item())
-    value = world * NEW / step_s
+    value = world * new / step_s
 
     # end to end through the host-buffer API: reset + prefill(host prompt) + decode(n, host tokens)
     e2e_times = []
-    host_out = np.empty(NEW, dtype=np.int32)
+    host_out = np.empty(new, dtype=np.int32)
     for i in range(args.warmup + args.steps):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         dec.reset()
         dec.prefill(prompt)
-        host_out[:] = dec.decode(NEW)
+        host_out[:] = dec.decode(new)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             e2e_times.append(dt)
@@ -242,27 +252,27 @@ def main():
         e2e_step = float(t.item())
 
     peaks, peak_kind = measured_peaks()
-    bytes_launch = algorithmic_bytes(TWO_B, PROMPT, NEW)
+    bytes_launch = algorithmic_bytes(model, prompt_len, new)
     achieved = bytes_launch / step_s / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "prompt": PROMPT, "decode_tokens": NEW, "weights": "fp16",
+        "config": {"workload": workload, "prompt": prompt_len, "decode_tokens": new, "weights": "fp16",
                    "kv_cache": "fp16", "l2": "no flush: 3.9 GB of weights (> 129 MB L2) streamed per token",
                    "parallelism": "replicas" if world > 1 else "single GPU", "n_cta": dec.n_cta},
-        "e2e": {"value": world * NEW / e2e_step, "unit": "tok/s", "h2d_bytes_per_step": PROMPT * 4,
-                "d2h_bytes_per_step": NEW * 4 + 8,
-                "timed": "reset + prefill(128-token host prompt) + decode(1024 -> host array), wall clock"},
+        "e2e": {"value": world * new / e2e_step, "unit": "tok/s", "h2d_bytes_per_step": prompt_len * 4,
+                "d2h_bytes_per_step": new * 4 + 8,
+                "timed": f"reset + prefill({prompt_len}-token host prompt) + decode({new} -> host array), wall clock"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": bytes_launch},
         "mbu": {"measured_peak": achieved / peaks["hbm_gbs"], "spec_8tbs": achieved / 8000.0},
-        "barriers": {"per_token": stats["barriers"] / NEW, "mean_latency_ns": stats["mean_latency_ns"],
+        "barriers": {"per_token": stats["barriers"] / new, "mean_latency_ns": stats["mean_latency_ns"],
                      "mean_wait_ns": stats["mean_wait_ns"],
-                     "wait_us_per_token": stats["mean_wait_ns"] * stats["barriers"] / NEW / 1e3},
+                     "wait_us_per_token": stats["mean_wait_ns"] * stats["barriers"] / new / 1e3},
         "clocks": clk,
     }
     dec.close()

@@ -72,7 +72,10 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   pl->n_cta = n_cta;
   if (n_cta < c->n_kv_heads) return "the grid needs at least one CTA per KV head";
   // shared memory: ring + input vector (largest of d, F, Hq*dh, attention scratch) + row results
-  const int att = G * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + kie::NCW * G * dh;
+  // attention scratch (floats): q [G][dh] f32, K and V sub-chunks [ATT_SUB][dh] f16, scores [G][ATT_SUB],
+  // 3 x MAX_GROUP running values, and the merge's [smax][G] m/weight and l arrays
+  const int smax = std::max(1, n_cta / c->n_kv_heads);
+  const int att = G * dh + kie::ATT_SUB * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
   pl->vec_floats = std::max(std::max(d, c->ffn_dim), std::max(dq, att));
   pl->out_floats = std::max(std::max(max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta),
                                      max_rows_per_cta(d, n_cta)),

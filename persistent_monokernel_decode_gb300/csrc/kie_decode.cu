@@ -113,82 +113,114 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 
 // ---- split-KV attention -----------------------------------------------------------------------------------
 
-// Piece `sp` of KV head `g`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial
-// (m, l, o) of each of the `group` query heads; the last piece of head g to finish merges all pieces
-// (log-sum-exp rescaling) into p.o. This is the pages' "attention recompute" idea in GB300 form: each SM
-// recomputes exactly its slice from the cache instead of exchanging intermediate attention state.
+// Piece `sp` of KV head `g`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial (m, l, o)
+// of each of the `group` query heads; the last piece of head g to finish merges all pieces (log-sum-exp
+// rescaling) into p.o. This is the pages' "attention recompute" idea in GB300 form: each SM recomputes exactly
+// its slice from the cache instead of exchanging intermediate attention state.
+//
+// Latency matters more than bandwidth here (a piece reads <= 16 KB of K/V per sub-chunk), so every sub-chunk's
+// K and V rows are requested together with q in one round trip, the next sub-chunk is prefetched into registers
+// while the current one is used from shared memory, and no step waits on a dependent global load.
 template <int DPL>
 __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, int g, int sp, int S, int j0,
                                        int j1) {
   constexpr int DH = DPL * 32;
+  constexpr int U = DH / 8;                          // 16-byte units per K or V row
+  constexpr int UPT = (ATT_SUB * U + NCT - 1) / NCT;  // units per thread per sub-chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.Hq / p.Hkv;
-  float *qs = s.vec;                      // [G][DH]
-  float *ps = qs + G * DH;                // [G][ATT_SUB]
-  float *corr = ps + G * ATT_SUB;         // [G]
-  float *mrun = corr + MAX_GROUP;         // [G]
-  float *lrun = mrun + MAX_GROUP;         // [G]
-  float *red = lrun + MAX_GROUP;          // [NCW][G][DH]
+  float *qs = s.vec;                                   // [G][DH]
+  __half *Ks = reinterpret_cast<__half *>(qs + G * DH);  // [ATT_SUB][DH]
+  __half *Vs = Ks + ATT_SUB * DH;                      // [ATT_SUB][DH]
+  float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * DH);  // [G][ATT_SUB]
+  float *corr = ps + G * ATT_SUB;                      // [MAX_GROUP]
+  float *mrun = corr + MAX_GROUP;
+  float *lrun = mrun + MAX_GROUP;
+  float *mw = lrun + MAX_GROUP;                        // merge: [smax][G] m, then weights
+  float *ml = mw + p.smax * G;                         // merge: [smax][G] l
   const float scale = 1.0f / sqrtf((float)DH);
-
-  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i);
-  if (tid < G) {
-    mrun[tid] = -INFINITY;
-    lrun[tid] = 0.f;
-  }
-  consumer_sync();
-
   const size_t plane = (size_t)p.max_seq * DH;
   const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + g) * plane;
   const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + g) * plane;
 
-  float acc[MAX_GROUP][DPL];
+  uint4 kreg[UPT], vreg[UPT];
+  auto fetch = [&](int jb) {  // registers <- K, V rows [jb, jb + ATT_SUB) that exist
+    const int nb = min(ATT_SUB, j1 - jb);
 #pragma unroll
-  for (int h = 0; h < MAX_GROUP; ++h)
+    for (int k = 0; k < UPT; ++k) {
+      const int u = tid + k * NCT;
+      if (u < nb * U) {
+        const size_t off = (size_t)(jb + u / U) * DH + (u % U) * 8;
+        kreg[k] = __ldcg(reinterpret_cast<const uint4 *>(Kb + off));
+        vreg[k] = __ldcg(reinterpret_cast<const uint4 *>(Vb + off));
+      }
+    }
+  };
+  auto stash = [&](int jb) {  // shared memory <- the registers fetched for jb
+    const int nb = min(ATT_SUB, j1 - jb);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+    for (int k = 0; k < UPT; ++k) {
+      const int u = tid + k * NCT;
+      if (u < nb * U) {
+        *reinterpret_cast<uint4 *>(Ks + (size_t)u * 8) = kreg[k];
+        *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = vreg[k];
+      }
+    }
+  };
+
+  if (j0 < j1) fetch(j0);
+  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i);
+  if (tid < MAX_GROUP) {
+    mrun[tid] = -INFINITY;
+    lrun[tid] = 0.f;
+  }
+  // each thread owns output pairs (h, d), (h, d + 1): o[k] for pair index tid + k * NCT
+  constexpr int OPT = (MAX_GROUP * DH / 2 + NCT - 1) / NCT;
+  float2 o[OPT];
+#pragma unroll
+  for (int k = 0; k < OPT; ++k) o[k] = make_float2(0.f, 0.f);
 
   for (int jb = j0; jb < j1; jb += ATT_SUB) {
     const int nb = min(ATT_SUB, j1 - jb);
-    // scores s = q . k / sqrt(dh): one warp per position, DPL dims per lane
-    for (int jj = warp; jj < nb; jj += NCW) {
-      const __half *kr = Kb + (size_t)(jb + jj) * DH + lane * DPL;
-      float kf[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 raw = __ldcg(reinterpret_cast<const uint2 *>(kr));
-        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        kf[0] = k0.x; kf[1] = k0.y; kf[2] = k1.x; kf[3] = k1.y;
-      } else {
-        const unsigned raw = __ldcg(reinterpret_cast<const unsigned *>(kr));
-        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
-        kf[0] = k0.x; kf[1] = k0.y;
+    stash(jb);
+    consumer_sync();                               // Ks, Vs (and qs) ready; ps free
+    if (jb + ATT_SUB < j1) fetch(jb + ATT_SUB);    // next sub-chunk in flight while this one is used
+    // scores: 8 lanes per position (DH/8 dims each), 4 positions per warp, reduce over the 8 lanes. Lanes past
+    // the last position compute on zeros so every lane runs the same shuffles; only their write is skipped.
+    {
+      const int jj = warp * 4 + (lane >> 3), sub = lane & 7;
+      const bool valid = jj < nb;
+      float kf[DH / 8];
+      const __half2 *kr = reinterpret_cast<const __half2 *>(Ks + (size_t)(valid ? jj : 0) * DH + sub * (DH / 8));
+#pragma unroll
+      for (int e = 0; e < DH / 16; ++e) {
+        const float2 f = valid ? __half22float2(kr[e]) : make_float2(0.f, 0.f);
+        kf[2 * e] = f.x;
+        kf[2 * e + 1] = f.y;
       }
 #pragma unroll
       for (int h = 0; h < MAX_GROUP; ++h) {
         if (h < G) {
+          const float *qh = qs + h * DH + sub * (DH / 8);
           float d = 0.f;
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) d = fmaf(kf[e], qs[h * DH + lane * DPL + e], d);
-          d = warp_sum(d);
-          if (lane == 0) ps[h * ATT_SUB + jj] = d * scale;
+          for (int e = 0; e < DH / 8; ++e) d = fmaf(kf[e], qh[e], d);
+          d += __shfl_xor_sync(0xffffffffu, d, 1);
+          d += __shfl_xor_sync(0xffffffffu, d, 2);
+          d += __shfl_xor_sync(0xffffffffu, d, 4);
+          if (sub == 0 && valid) ps[h * ATT_SUB + jj] = d * scale;
         }
       }
     }
     consumer_sync();
-    // online softmax: one warp per query head
-    for (int h = warp; h < G; h += NCW) {
-      float mx = -INFINITY;
-      for (int jj = lane; jj < nb; jj += 32) mx = fmaxf(mx, ps[h * ATT_SUB + jj]);
-      mx = warp_max(mx);
-      const float mnew = fmaxf(mrun[h], mx);
-      float sum = 0.f;
-      for (int jj = lane; jj < nb; jj += 32) {
-        const float e = expf(ps[h * ATT_SUB + jj] - mnew);
-        ps[h * ATT_SUB + jj] = e;
-        sum += e;
-      }
-      sum = warp_sum(sum);
+    // online softmax: warp h owns head h, lane j position j of the sub-chunk
+    if (warp < G) {
+      const int h = warp;
+      const float sc = lane < nb ? ps[h * ATT_SUB + lane] : -INFINITY;
+      const float mnew = fmaxf(mrun[h], warp_max(sc));
+      const float e = lane < nb ? expf(sc - mnew) : 0.f;
+      ps[h * ATT_SUB + lane] = e;
+      const float sum = warp_sum(e);
       if (lane == 0) {
         const float c = expf(mrun[h] - mnew);
         corr[h] = c;
@@ -197,51 +229,32 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       }
     }
     consumer_sync();
-    // o += p v, after rescaling what this warp accumulated so far
+    // o = o * corr + P V over this sub-chunk
 #pragma unroll
-    for (int h = 0; h < MAX_GROUP; ++h)
-      if (h < G) {
+    for (int k = 0; k < OPT; ++k) {
+      const int pr = tid + k * NCT;
+      if (pr < G * DH / 2) {
+        const int h = (2 * pr) / DH, d = (2 * pr) % DH;
         const float c = corr[h];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[h][e] *= c;
-      }
-    for (int jj = warp; jj < nb; jj += NCW) {
-      const __half *vr = Vb + (size_t)(jb + jj) * DH + lane * DPL;
-      float vf[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 raw = __ldcg(reinterpret_cast<const uint2 *>(vr));
-        const float2 v0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 v1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        vf[0] = v0.x; vf[1] = v0.y; vf[2] = v1.x; vf[3] = v1.y;
-      } else {
-        const unsigned raw = __ldcg(reinterpret_cast<const unsigned *>(vr));
-        const float2 v0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
-        vf[0] = v0.x; vf[1] = v0.y;
-      }
-#pragma unroll
-      for (int h = 0; h < MAX_GROUP; ++h)
-        if (h < G) {
-          const float pj = ps[h * ATT_SUB + jj];
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[h][e] = fmaf(pj, vf[e], acc[h][e]);
+        float ax = o[k].x * c, ay = o[k].y * c;
+        const float *ph = ps + h * ATT_SUB;
+        for (int jj = 0; jj < nb; ++jj) {
+          const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(Vs + (size_t)jj * DH + d));
+          ax = fmaf(ph[jj], v.x, ax);
+          ay = fmaf(ph[jj], v.y, ay);
         }
+        o[k] = make_float2(ax, ay);
+      }
     }
-    consumer_sync();
+    consumer_sync();                               // Ks, Vs, ps reused by the next sub-chunk
   }
 
-  // cross-warp sum of the partial outputs, then publish (m, l, o) of this piece
-#pragma unroll
-  for (int h = 0; h < MAX_GROUP; ++h)
-    if (h < G)
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) red[((size_t)warp * G + h) * DH + lane * DPL + e] = acc[h][e];
-  consumer_sync();
+  // publish (m, l, o) of this piece
   const size_t piece = (size_t)g * p.smax + sp;
-  for (int i = tid; i < G * DH; i += NCT) {
-    float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < NCW; ++w) t += red[(size_t)w * G * DH + i];
-    p.part_o[piece * G * DH + i] = t;
+  for (int k = 0; k < OPT; ++k) {
+    const int pr = tid + k * NCT;
+    if (pr < G * DH / 2) *reinterpret_cast<float2 *>(p.part_o + piece * G * DH + 2 * pr) = o[k];
   }
   if (tid < G) {
     p.part_ml[(piece * G + tid) * 2] = mrun[tid];
@@ -259,20 +272,52 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     s.flags[1] = last;
   }
   consumer_sync();
-  if (s.flags[1]) {
-    for (int i = tid; i < G * DH; i += NCT) {
-      const int h = i / DH;
-      float M = -INFINITY;
-      for (int q = 0; q < S; ++q) M = fmaxf(M, __ldcg(p.part_ml + (((size_t)g * p.smax + q) * G + h) * 2));
-      float num = 0.f, den = 0.f;
-      for (int q = 0; q < S; ++q) {
-        const size_t pc = (size_t)g * p.smax + q;
-        const float w = expf(__ldcg(p.part_ml + (pc * G + h) * 2) - M);
-        den = fmaf(w, __ldcg(p.part_ml + (pc * G + h) * 2 + 1), den);
-        num = fmaf(w, __ldcg(p.part_o + pc * G * DH + i), num);
-      }
-      p.o[(size_t)g * G * DH + i] = num / den;
+  if (!s.flags[1]) return;
+
+  // last piece of this KV head: merge the S pieces. Weights w[q][h] = exp(m_q - M_h) / sum_q exp(m_q - M_h) l_q.
+  float *wgt = mw;
+  for (int i = tid; i < S * G; i += NCT) {
+    const size_t pc = (size_t)g * p.smax + i / G;
+    wgt[i] = __ldcg(p.part_ml + (pc * G + i % G) * 2);
+    ml[i] = __ldcg(p.part_ml + (pc * G + i % G) * 2 + 1);
+  }
+  consumer_sync();
+  if (tid < G) {
+    float M = -INFINITY;
+    for (int q = 0; q < S; ++q) M = fmaxf(M, wgt[q * G + tid]);
+    float den = 0.f;
+    for (int q = 0; q < S; ++q) {
+      const float w = expf(wgt[q * G + tid] - M);
+      wgt[q * G + tid] = w;
+      den = fmaf(w, ml[q * G + tid], den);
     }
+    corr[tid] = 1.0f / den;
+  }
+  consumer_sync();
+  for (int pr = tid; pr < G * DH / 2; pr += NCT) {
+    const int h = (2 * pr) / DH;
+    float ax = 0.f, ay = 0.f;
+    int q = 0;
+    for (; q + 4 <= S; q += 4) {
+      float2 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        v[u] = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q + u) * G * DH + 2 * pr));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = wgt[(q + u) * G + h];
+        ax = fmaf(w, v[u].x, ax);
+        ay = fmaf(w, v[u].y, ay);
+      }
+    }
+    for (; q < S; ++q) {
+      const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q) * G * DH + 2 * pr));
+      const float w = wgt[q * G + h];
+      ax = fmaf(w, v.x, ax);
+      ay = fmaf(w, v.y, ay);
+    }
+    const float inv = corr[h];
+    *reinterpret_cast<float2 *>(p.o + (size_t)g * G * DH + 2 * pr) = make_float2(ax * inv, ay * inv);
   }
 }
 
