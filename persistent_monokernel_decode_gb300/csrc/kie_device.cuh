@@ -275,11 +275,18 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 xa, const floa
 // producer streams for this region. A thread whose wait gives up raises the CTA abort flag and skips the
 // remaining waits, but walks the same tile sequence, so every consumer thread still reaches the same
 // named barriers; callers test the flag only after a consumer_sync, where it is CTA-uniform.
-__device__ inline void consume_region(Smem &s, int nslot, RingPos &rp, int R, int K, float scale,
+static __device__ __noinline__ void consume_region(Smem &s, int nslot, RingPos &rp, int R, int K, float scale,
                                       const Guard &g) {
   bool ok = s.flags[0] == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // register copies of the shared-memory layout (the struct itself may live in local memory here)
   const float *vec = s.vec;
+  uint8_t *const ring = s.ring;
+  uint64_t *const full = s.full, *const empty = s.empty;
+  float *const out = s.out;
+  volatile int *const flags = s.flags;
+  int slot = rp.slot;
+  uint32_t phase = rp.phase;
   for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
     const int rows = min(TILE_ROWS, R - g0);
     float acc[ROWS_PER_WARP];
@@ -287,36 +294,47 @@ __device__ inline void consume_region(Smem &s, int nslot, RingPos &rp, int R, in
     for (int j = 0; j < ROWS_PER_WARP; ++j) acc[j] = 0.f;
     for (int k0 = 0; k0 < K; k0 += TILE_COLS) {
       const int w = min(TILE_COLS, K - k0);
-      if (ok && !wait_mbar(&s.full[rp.slot], rp.phase, g)) {
+      if (ok && !wait_mbar(&full[slot], phase, g)) {
         ok = false;
-        s.flags[0] = 1;
+        flags[0] = 1;
       }
-      if (ok && lane * 8 < w) {
-        const uint8_t *tile = s.ring + (size_t)rp.slot * SLOT_BYTES;
-        const float4 xa = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8);
-        const float4 xb = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8 + 4);
+      // copy this warp's rows of the tile to registers and hand the slot back before doing the math, so a
+      // slot is held only for the shared-memory reads and the producer can refill it sooner
+      const bool active = ok && lane * 8 < w;
+      uint4 wv[ROWS_PER_WARP];
+      if (active) {
+        const uint8_t *tile = ring + (size_t)slot * SLOT_BYTES;
 #pragma unroll
         for (int j = 0; j < ROWS_PER_WARP; ++j) {
           const int r = warp + NCW * j;
-          if (r < rows) {
-            const uint4 wv = *reinterpret_cast<const uint4 *>(tile + ((size_t)r * w + lane * 8) * 2);
-            acc[j] += dot8(wv, xa, xb);
-          }
+          if (r < rows) wv[j] = *reinterpret_cast<const uint4 *>(tile + ((size_t)r * w + lane * 8) * 2);
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.empty[rp.slot]);
-      ring_advance(rp, nslot);
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (++slot == nslot) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (active) {
+        const float4 xa = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8);
+        const float4 xb = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8 + 4);
+#pragma unroll
+        for (int j = 0; j < ROWS_PER_WARP; ++j)
+          if (warp + NCW * j < rows) acc[j] += dot8(wv[j], xa, xb);
+      }
     }
 #pragma unroll
     for (int j = 0; j < ROWS_PER_WARP; ++j) {
       const int r = warp + NCW * j;
       if (r < rows) {
         const float v = warp_sum(acc[j]);
-        if (lane == 0) s.out[g0 + r] = v * scale;
+        if (lane == 0) out[g0 + r] = v * scale;
       }
     }
   }
+  rp.slot = slot;
+  rp.phase = phase;
 }
 
 // ---- staging the input vector ---------------------------------------------------------------------------
