@@ -271,44 +271,88 @@ __device__ __forceinline__ float dot8(const uint4 w, const float4 xa, const floa
   return a + b;
 }
 
-// out[i] = scale * sum_k W[r0 + i][k] * vec[k] for the R rows of this CTA, consuming the tiles the
-// producer streams for this region. A thread whose wait gives up raises the CTA abort flag and skips the
-// remaining waits, but walks the same tile sequence, so every consumer thread still reaches the same
-// named barriers; callers test the flag only after a consumer_sync, where it is CTA-uniform.
+// The column blocks [k_begin, k_end) (full 256-column blocks) of one row group, for a warp that owns NJ rows of
+// the group (rows warp, warp + NCW, ...). Every warp waits for and releases every tile, whatever its NJ: the
+// ring's empty barriers count NCW arrivals. The warp copies its rows to registers and hands the slot back
+// before the math, so a slot is held only for the shared-memory reads. This loop is kept free of per-row
+// guards and runtime strides: it is the hot loop of the whole decode.
+template <int NJ>
+__device__ __forceinline__ void tile_loop(const uint8_t *ring, uint64_t *full, uint64_t *empty, const float *vec,
+                                          float (&acc)[ROWS_PER_WARP], int nslot, int &slot, uint32_t &phase,
+                                          int k_begin, int k_end, bool &ok, volatile int *flags, const Guard &g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k0 = k_begin; k0 < k_end; k0 += TILE_COLS) {
+    if (ok && !wait_mbar(&full[slot], phase, g)) {
+      ok = false;
+      flags[0] = 1;
+    }
+    // no branch on `ok` here: after an abort the reads below still stay inside the slot and the results are
+    // discarded, and a branch-free body is what lets the compiler overlap one tile's reads with the math
+    uint4 wv[NJ > 0 ? NJ : 1];
+    const uint8_t *t = ring + (size_t)slot * SLOT_BYTES + (size_t)warp * (TILE_COLS * 2) + lane * 16;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) wv[j] = *reinterpret_cast<const uint4 *>(t + (size_t)j * NCW * TILE_COLS * 2);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == nslot) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (NJ > 0) {
+      const float4 xa = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8);
+      const float4 xb = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8 + 4);
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) acc[j] += dot8(wv[j], xa, xb);
+    }
+  }
+}
+
+// out[i] = scale * sum_k W[r0 + i][k] * vec[k] for the R rows of this CTA, consuming the tiles the producer
+// streams for this region (row group by row group, each group column block by column block). Warp w owns rows
+// w, w + NCW, ... of each group and reduces them across lanes at the end of the group.
+//
+// A thread whose wait gives up raises the CTA abort flag and skips the remaining waits but walks the same tile
+// sequence, so every consumer thread reaches the same named barriers; callers test the flag only after a
+// consumer_sync.
 static __device__ __noinline__ void consume_region(Smem &s, int nslot, RingPos &rp, int R, int K, float scale,
-                                      const Guard &g) {
+                                                   const Guard &g) {
   bool ok = s.flags[0] == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // register copies of the shared-memory layout (the struct itself may live in local memory here)
   const float *vec = s.vec;
-  uint8_t *const ring = s.ring;
+  const uint8_t *const ring = s.ring;
   uint64_t *const full = s.full, *const empty = s.empty;
   float *const out = s.out;
   volatile int *const flags = s.flags;
   int slot = rp.slot;
   uint32_t phase = rp.phase;
+  const int kfull = K / TILE_COLS * TILE_COLS;  // columns covered by full 256-column blocks
   for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
     const int rows = min(TILE_ROWS, R - g0);
+    const int nj = min(ROWS_PER_WARP, (rows - warp + NCW - 1) / NCW);  // rows of this group owned by the warp
     float acc[ROWS_PER_WARP];
 #pragma unroll
     for (int j = 0; j < ROWS_PER_WARP; ++j) acc[j] = 0.f;
-    for (int k0 = 0; k0 < K; k0 += TILE_COLS) {
-      const int w = min(TILE_COLS, K - k0);
+    switch (nj) {
+      case 4: tile_loop<4>(ring, full, empty, vec, acc, nslot, slot, phase, 0, kfull, ok, flags, g); break;
+      case 3: tile_loop<3>(ring, full, empty, vec, acc, nslot, slot, phase, 0, kfull, ok, flags, g); break;
+      case 2: tile_loop<2>(ring, full, empty, vec, acc, nslot, slot, phase, 0, kfull, ok, flags, g); break;
+      case 1: tile_loop<1>(ring, full, empty, vec, acc, nslot, slot, phase, 0, kfull, ok, flags, g); break;
+      default: tile_loop<0>(ring, full, empty, vec, acc, nslot, slot, phase, 0, kfull, ok, flags, g); break;
+    }
+    if (kfull < K) {  // a last, narrower column block (K not a multiple of 256): the guarded path
+      const int k0 = kfull, w = K - kfull;
       if (ok && !wait_mbar(&full[slot], phase, g)) {
         ok = false;
         flags[0] = 1;
       }
-      // copy this warp's rows of the tile to registers and hand the slot back before doing the math, so a
-      // slot is held only for the shared-memory reads and the producer can refill it sooner
       const bool active = ok && lane * 8 < w;
       uint4 wv[ROWS_PER_WARP];
       if (active) {
         const uint8_t *tile = ring + (size_t)slot * SLOT_BYTES;
 #pragma unroll
-        for (int j = 0; j < ROWS_PER_WARP; ++j) {
-          const int r = warp + NCW * j;
-          if (r < rows) wv[j] = *reinterpret_cast<const uint4 *>(tile + ((size_t)r * w + lane * 8) * 2);
-        }
+        for (int j = 0; j < ROWS_PER_WARP; ++j)
+          if (j < nj) wv[j] = *reinterpret_cast<const uint4 *>(tile + ((size_t)(warp + NCW * j) * w + lane * 8) * 2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
@@ -321,15 +365,14 @@ static __device__ __noinline__ void consume_region(Smem &s, int nslot, RingPos &
         const float4 xb = *reinterpret_cast<const float4 *>(vec + k0 + lane * 8 + 4);
 #pragma unroll
         for (int j = 0; j < ROWS_PER_WARP; ++j)
-          if (warp + NCW * j < rows) acc[j] += dot8(wv[j], xa, xb);
+          if (j < nj) acc[j] += dot8(wv[j], xa, xb);
       }
     }
 #pragma unroll
     for (int j = 0; j < ROWS_PER_WARP; ++j) {
-      const int r = warp + NCW * j;
-      if (r < rows) {
+      if (j < nj) {
         const float v = warp_sum(acc[j]);
-        if (lane == 0) out[g0 + r] = v * scale;
+        if (lane == 0) out[g0 + warp + NCW * j] = v * scale;
       }
     }
   }
