@@ -129,7 +129,7 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   constexpr int UPT = (ATT_SUB * U + NCT - 1) / NCT;  // units per thread per sub-chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.Hq / p.Hkv;
-  float *qs = s.vec;                                   // [G][DH]
+  float *qs = s.vec;                                   // [G][DH], pre-scaled by 1/sqrt(dh)
   __half *Ks = reinterpret_cast<__half *>(qs + G * DH);  // [ATT_SUB][DH]
   __half *Vs = Ks + ATT_SUB * DH;                      // [ATT_SUB][DH]
   float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * DH);  // [G][ATT_SUB]
@@ -156,20 +156,24 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       }
     }
   };
-  auto stash = [&](int jb) {  // shared memory <- the registers fetched for jb
+  // shared memory <- the registers fetched for jb; rows past the end are zero, so that the score and P.V loops
+  // below can always run over ATT_SUB positions without guards
+  auto stash = [&](int jb) {
     const int nb = min(ATT_SUB, j1 - jb);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
       const int u = tid + k * NCT;
-      if (u < nb * U) {
-        *reinterpret_cast<uint4 *>(Ks + (size_t)u * 8) = kreg[k];
-        *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = vreg[k];
+      if (u < ATT_SUB * U) {
+        const bool in = u < nb * U;
+        *reinterpret_cast<uint4 *>(Ks + (size_t)u * 8) = in ? kreg[k] : zero;
+        *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = in ? vreg[k] : zero;
       }
     }
   };
 
   if (j0 < j1) fetch(j0);
-  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i);
+  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i) * scale;
   if (tid < MAX_GROUP) {
     mrun[tid] = -INFINITY;
     lrun[tid] = 0.f;
@@ -185,35 +189,45 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     stash(jb);
     consumer_sync();                               // Ks, Vs (and qs) ready; ps free
     if (jb + ATT_SUB < j1) fetch(jb + ATT_SUB);    // next sub-chunk in flight while this one is used
-    // scores: 8 lanes per position (DH/8 dims each), 4 positions per warp, reduce over the 8 lanes. Lanes past
-    // the last position compute on zeros so every lane runs the same shuffles; only their write is skipped.
+    // scores: 8 lanes per position (DH/8 dims each), 4 positions per warp, reduce over the 8 lanes
     {
       const int jj = warp * 4 + (lane >> 3), sub = lane & 7;
-      const bool valid = jj < nb;
       float kf[DH / 8];
-      const __half2 *kr = reinterpret_cast<const __half2 *>(Ks + (size_t)(valid ? jj : 0) * DH + sub * (DH / 8));
+      const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)jj * DH + sub * (DH / 8));
 #pragma unroll
-      for (int e = 0; e < DH / 16; ++e) {
-        const float2 f = valid ? __half22float2(kr[e]) : make_float2(0.f, 0.f);
-        kf[2 * e] = f.x;
-        kf[2 * e + 1] = f.y;
+      for (int v = 0; v < DH / 64; ++v) {
+        const uint4 raw = kr[v];
+        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h2[e]);
+          kf[8 * v + 2 * e] = f.x;
+          kf[8 * v + 2 * e + 1] = f.y;
+        }
       }
 #pragma unroll
       for (int h = 0; h < MAX_GROUP; ++h) {
         if (h < G) {
-          const float *qh = qs + h * DH + sub * (DH / 8);
-          float d = 0.f;
+          const float4 *qh = reinterpret_cast<const float4 *>(qs + h * DH + sub * (DH / 8));
+          float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-          for (int e = 0; e < DH / 8; ++e) d = fmaf(kf[e], qh[e], d);
+          for (int v = 0; v < DH / 32; ++v) {
+            const float4 q4 = qh[v];
+            d0 = fmaf(kf[4 * v], q4.x, d0);
+            d1 = fmaf(kf[4 * v + 1], q4.y, d1);
+            d0 = fmaf(kf[4 * v + 2], q4.z, d0);
+            d1 = fmaf(kf[4 * v + 3], q4.w, d1);
+          }
+          float d = d0 + d1;
           d += __shfl_xor_sync(0xffffffffu, d, 1);
           d += __shfl_xor_sync(0xffffffffu, d, 2);
           d += __shfl_xor_sync(0xffffffffu, d, 4);
-          if (sub == 0 && valid) ps[h * ATT_SUB + jj] = d * scale;
+          if (sub == 0 && jj < nb) ps[h * ATT_SUB + jj] = d;
         }
       }
     }
     consumer_sync();
-    // online softmax: warp h owns head h, lane j position j of the sub-chunk
+    // online softmax: warp h owns head h, lane j position j of the sub-chunk (positions past nb weigh 0)
     if (warp < G) {
       const int h = warp;
       const float sc = lane < nb ? ps[h * ATT_SUB + lane] : -INFINITY;
@@ -229,21 +243,24 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       }
     }
     consumer_sync();
-    // o = o * corr + P V over this sub-chunk
+    // o = o * corr + P V over this sub-chunk: a fixed ATT_SUB steps (zero rows past nb), 4 independent sums
 #pragma unroll
     for (int k = 0; k < OPT; ++k) {
       const int pr = tid + k * NCT;
       if (pr < G * DH / 2) {
         const int h = (2 * pr) / DH, d = (2 * pr) % DH;
-        const float c = corr[h];
-        float ax = o[k].x * c, ay = o[k].y * c;
         const float *ph = ps + h * ATT_SUB;
-        for (int jj = 0; jj < nb; ++jj) {
+        float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int jj = 0; jj < ATT_SUB; ++jj) {
           const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(Vs + (size_t)jj * DH + d));
-          ax = fmaf(ph[jj], v.x, ax);
-          ay = fmaf(ph[jj], v.y, ay);
+          const float pj = ph[jj];
+          a[jj & 3].x = fmaf(pj, v.x, a[jj & 3].x);
+          a[jj & 3].y = fmaf(pj, v.y, a[jj & 3].y);
         }
-        o[k] = make_float2(ax, ay);
+        const float c = corr[h];
+        o[k].x = o[k].x * c + ((a[0].x + a[1].x) + (a[2].x + a[3].x));
+        o[k].y = o[k].y * c + ((a[0].y + a[1].y) + (a[2].y + a[3].y));
       }
     }
     consumer_sync();                               // Ks, Vs, ps reused by the next sub-chunk
@@ -274,7 +291,22 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   consumer_sync();
   if (!s.flags[1]) return;
 
-  // last piece of this KV head: merge the S pieces. Weights w[q][h] = exp(m_q - M_h) / sum_q exp(m_q - M_h) l_q.
+  // Last piece of this KV head: merge the S pieces, o_h = sum_q w_q o_q / sum_q w_q l_q with
+  // w_q = exp(m_q - max m). The first batch of partial outputs is requested before the (m, l) values, so both
+  // round trips overlap.
+  constexpr int MB = 4;  // pieces per batch of loads
+  float2 v[OPT][MB];
+  auto load_batch = [&](int q0) {
+#pragma unroll
+    for (int k = 0; k < OPT; ++k) {
+      const int pr = tid + k * NCT;
+#pragma unroll
+      for (int u = 0; u < MB; ++u)
+        if (pr < G * DH / 2 && q0 + u < S)
+          v[k][u] = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q0 + u) * G * DH + 2 * pr));
+    }
+  };
+  load_batch(0);
   float *wgt = mw;
   for (int i = tid; i < S * G; i += NCT) {
     const size_t pc = (size_t)g * p.smax + i / G;
@@ -294,38 +326,44 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     corr[tid] = 1.0f / den;
   }
   consumer_sync();
-  for (int pr = tid; pr < G * DH / 2; pr += NCT) {
-    const int h = (2 * pr) / DH;
-    float ax = 0.f, ay = 0.f;
-    int q = 0;
-    for (; q + 4 <= S; q += 4) {
-      float2 v[4];
+  float2 acc[OPT];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        v[u] = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q + u) * G * DH + 2 * pr));
+  for (int k = 0; k < OPT; ++k) acc[k] = make_float2(0.f, 0.f);
+  for (int q0 = 0; q0 < S; q0 += MB) {
+    if (q0 > 0) load_batch(q0);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = wgt[(q + u) * G + h];
-        ax = fmaf(w, v[u].x, ax);
-        ay = fmaf(w, v[u].y, ay);
+    for (int k = 0; k < OPT; ++k) {
+      const int pr = tid + k * NCT;
+      if (pr < G * DH / 2) {
+        const int h = (2 * pr) / DH;
+#pragma unroll
+        for (int u = 0; u < MB; ++u)
+          if (q0 + u < S) {
+            const float w = wgt[(q0 + u) * G + h];
+            acc[k].x = fmaf(w, v[k][u].x, acc[k].x);
+            acc[k].y = fmaf(w, v[k][u].y, acc[k].y);
+          }
       }
     }
-    for (; q < S; ++q) {
-      const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q) * G * DH + 2 * pr));
-      const float w = wgt[q * G + h];
-      ax = fmaf(w, v.x, ax);
-      ay = fmaf(w, v.y, ay);
+  }
+#pragma unroll
+  for (int k = 0; k < OPT; ++k) {
+    const int pr = tid + k * NCT;
+    if (pr < G * DH / 2) {
+      const float inv = corr[(2 * pr) / DH];
+      *reinterpret_cast<float2 *>(p.o + (size_t)g * G * DH + 2 * pr) = make_float2(acc[k].x * inv, acc[k].y * inv);
     }
-    const float inv = corr[h];
-    *reinterpret_cast<float2 *>(p.o + (size_t)g * G * DH + 2 * pr) = make_float2(ax * inv, ay * inv);
   }
 }
 
 // ---- the kernel -------------------------------------------------------------------------------------------
 
+// Pieces per KV head for c attended positions: one sub-chunk (ATT_SUB positions) per piece while there are
+// enough CTAs, at most smax so that every piece has its own CTA (longer contexts then give each piece several
+// sub-chunks). Fewer, longer pieces measured slower: the sub-chunks of a piece run one after the other.
 __device__ __forceinline__ int split_pieces(const DecodeParams &p, int c) {
-  const int by_len = (c + ATT_MIN_CHUNK - 1) / ATT_MIN_CHUNK;
-  return by_len < p.smax ? by_len : p.smax;
+  const int s = (c + ATT_SUB - 1) / ATT_SUB;
+  return s < p.smax ? s : p.smax;
 }
 
 __device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard &g) {

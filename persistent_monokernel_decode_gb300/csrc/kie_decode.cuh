@@ -7,7 +7,6 @@ namespace kie {
 
 constexpr int MAX_GROUP = 8;         // query heads per KV head supported by the attention step
 constexpr int ATT_SUB = 32;          // positions per online-softmax sub-chunk (one lane each)
-constexpr int ATT_MIN_CHUNK = 32;    // fewest positions a split-KV CTA takes
 constexpr int MAX_KV_HEADS = 64;
 constexpr int TRACE_CAP = 4096;      // grid barriers whose per-CTA waits are recorded per launch
 
