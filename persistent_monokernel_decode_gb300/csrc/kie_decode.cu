@@ -6,7 +6,7 @@
 //
 //   embed -> for each layer:
 //     [QKV]   q,k,v = inv_rms(x) * (W'qkv x); RoPE from the table; K,V appended (fp16) ........ barrier
-//     [ATT]   split-KV attention over the cached positions; the last piece per KV head merges ... barrier
+//     [ATT]   split-KV attention over the cached positions; the pieces of a KV head merge it ...... barrier
 //     [WO]    h = x + Wo o ........................................................................ barrier
 //     [GU]    a = silu(gate) * up,  [gate; up] = inv_rms(h) * (W'gu h), rows interleaved ........ barrier
 //     [DOWN]  x = h + Wd a ........................................................................ barrier
@@ -113,17 +113,17 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 
 // ---- split-KV attention -----------------------------------------------------------------------------------
 
-// Piece `sp` of KV head `g`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial (m, l, o)
-// of each of the `group` query heads; the last piece of head g to finish merges all pieces (log-sum-exp
-// rescaling) into p.o. This is the pages' "attention recompute" idea in GB300 form: each SM recomputes exactly
+// Piece `sp` of KV head `kh`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial (m, l, o)
+// of each of the `group` query heads; once all S pieces of the head are in, each piece merges a 1/S slice of
+// the head's outputs (log-sum-exp rescaling) into p.o. This is the pages' "attention recompute" idea in GB300 form: each SM recomputes exactly
 // its slice from the cache instead of exchanging intermediate attention state.
 //
 // Latency matters more than bandwidth here (a piece reads <= 16 KB of K/V per sub-chunk), so every sub-chunk's
 // K and V rows are requested together with q in one round trip, the next sub-chunk is prefetched into registers
 // while the current one is used from shared memory, and no step waits on a dependent global load.
 template <int DPL>
-__device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, int g, int sp, int S, int j0,
-                                       int j1) {
+__device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, int kh, int sp, int S, int j0,
+                                       int j1, unsigned target, const Guard &g) {
   constexpr int DH = DPL * 32;
   constexpr int U = DH / 8;                          // 16-byte units per K or V row
   constexpr int UPT = (ATT_SUB * U + NCT - 1) / NCT;  // units per thread per sub-chunk
@@ -140,8 +140,8 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   float *ml = mw + p.smax * G;                         // merge: [smax][G] l
   const float scale = 1.0f / sqrtf((float)DH);
   const size_t plane = (size_t)p.max_seq * DH;
-  const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + g) * plane;
-  const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + g) * plane;
+  const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + kh) * plane;
+  const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + kh) * plane;
 
   uint4 kreg[UPT], vreg[UPT];
   auto fetch = [&](int jb) {  // registers <- K, V rows [jb, jb + ATT_SUB) that exist
@@ -173,7 +173,7 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   };
 
   if (j0 < j1) fetch(j0);
-  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)g * G * DH + i) * scale;
+  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)kh * G * DH + i) * scale;
   if (tid < MAX_GROUP) {
     mrun[tid] = -INFINITY;
     lrun[tid] = 0.f;
@@ -267,92 +267,94 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   }
 
   // publish (m, l, o) of this piece
-  const size_t piece = (size_t)g * p.smax + sp;
+  const int E = G * DH;  // outputs of this KV head's query group
+  const size_t piece = (size_t)kh * p.smax + sp;
 #pragma unroll
   for (int k = 0; k < OPT; ++k) {
     const int pr = tid + k * NCT;
-    if (pr < G * DH / 2) *reinterpret_cast<float2 *>(p.part_o + piece * G * DH + 2 * pr) = o[k];
+    if (pr < E / 2) *reinterpret_cast<float2 *>(p.part_o + piece * E + 2 * pr) = o[k];
   }
-  if (tid < G) {
-    p.part_ml[(piece * G + tid) * 2] = mrun[tid];
-    p.part_ml[(piece * G + tid) * 2 + 1] = lrun[tid];
-  }
+  if (tid < G) *reinterpret_cast<float2 *>(p.part_ml + (piece * G + tid) * 2) = make_float2(mrun[tid], lrun[tid]);
   consumer_sync();
+  // count this piece in (no reply needed), then wait for the other pieces of head kh: the counter only grows
+  // during a launch, and `target` is the running total of pieces up to this layer's attention step
   if (tid == 0) {
     __threadfence();
-    const unsigned old = atomicAdd(&p.ctl->att_cnt[g], 1u);
-    const int last = old == (unsigned)(S - 1);
-    if (last) {
-      p.ctl->att_cnt[g] = 0u;  // next use is a later layer, after several grid barriers
-      __threadfence();
-    }
-    s.flags[1] = last;
-  }
-  consumer_sync();
-  if (!s.flags[1]) return;
-
-  // Last piece of this KV head: merge the S pieces, o_h = sum_q w_q o_q / sum_q w_q l_q with
-  // w_q = exp(m_q - max m). The first batch of partial outputs is requested before the (m, l) values, so both
-  // round trips overlap.
-  constexpr int MB = 4;  // pieces per batch of loads
-  float2 v[OPT][MB];
-  auto load_batch = [&](int q0) {
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int pr = tid + k * NCT;
-#pragma unroll
-      for (int u = 0; u < MB; ++u)
-        if (pr < G * DH / 2 && q0 + u < S)
-          v[k][u] = __ldcg(reinterpret_cast<const float2 *>(p.part_o + ((size_t)g * p.smax + q0 + u) * G * DH + 2 * pr));
-    }
-  };
-  load_batch(0);
-  float *wgt = mw;
-  for (int i = tid; i < S * G; i += NCT) {
-    const size_t pc = (size_t)g * p.smax + i / G;
-    wgt[i] = __ldcg(p.part_ml + (pc * G + i % G) * 2);
-    ml[i] = __ldcg(p.part_ml + (pc * G + i % G) * 2 + 1);
-  }
-  consumer_sync();
-  if (tid < G) {
-    float M = -INFINITY;
-    for (int q = 0; q < S; ++q) M = fmaxf(M, wgt[q * G + tid]);
-    float den = 0.f;
-    for (int q = 0; q < S; ++q) {
-      const float w = expf(wgt[q * G + tid] - M);
-      wgt[q * G + tid] = w;
-      den = fmaf(w, ml[q * G + tid], den);
-    }
-    corr[tid] = 1.0f / den;
-  }
-  consumer_sync();
-  float2 acc[OPT];
-#pragma unroll
-  for (int k = 0; k < OPT; ++k) acc[k] = make_float2(0.f, 0.f);
-  for (int q0 = 0; q0 < S; q0 += MB) {
-    if (q0 > 0) load_batch(q0);
-#pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int pr = tid + k * NCT;
-      if (pr < G * DH / 2) {
-        const int h = (2 * pr) / DH;
-#pragma unroll
-        for (int u = 0; u < MB; ++u)
-          if (q0 + u < S) {
-            const float w = wgt[(q0 + u) * G + h];
-            acc[k].x = fmaf(w, v[k][u].x, acc[k].x);
-            acc[k].y = fmaf(w, v[k][u].y, acc[k].y);
-          }
+    atomicAdd(&p.ctl->att_cnt[kh], 1u);
+    const uint64_t t0 = globaltimer();
+    bool ok = true;
+    for (int spins = 1;; ++spins) {
+      if ((int)(ld_acquire_gpu(&p.ctl->att_cnt[kh]) - target) >= 0) break;
+      if ((spins & 15) == 0) {
+        if (ld_relaxed_gpu(&p.ctl->status) != ST_OK) {
+          ok = false;
+          break;
+        }
+        if (globaltimer() - t0 > p.timeout_ns) {
+          raise_status(g, ST_TIMEOUT);
+          ok = false;
+          break;
+        }
       }
     }
+    if (!ok) s.flags[0] = 1;
   }
+  consumer_sync();
+  if (s.flags[0]) return;
+
+  // Merge, split across the S pieces of the head: this CTA produces outputs [e0, e1) of the E,
+  //   o_e = sum_q w_q o_q,e   with   w_q = exp(m_q - M) / sum_r exp(m_r - M) l_r,   M = max_r m_r
+  // for the query head of e. Every value it needs (all (m, l) of the head, and its slice of every piece's o)
+  // is requested before any is used: one round trip.
+  const int sl = (E + S - 1) / S;
+  const int e0 = min(E, sp * sl), e1 = min(E, e0 + sl), w = e1 - e0;
+  if (w == 0) return;
+  float *mo = reinterpret_cast<float *>(Ks);  // [S][w] (the K/V staging area is free now)
+  constexpr int LPT = (MAX_GROUP * DH + NCT - 1) / NCT + 1;  // o loads per thread per round
+  for (int r = 0; r * LPT * NCT < S * w || r * NCT < S * G; ++r) {  // one round unless S * G > NCT
+    const int base = r * LPT * NCT;
+    float rv[LPT];
+    float2 rml;
 #pragma unroll
-  for (int k = 0; k < OPT; ++k) {
-    const int pr = tid + k * NCT;
-    if (pr < G * DH / 2) {
-      const float inv = corr[(2 * pr) / DH];
-      *reinterpret_cast<float2 *>(p.o + (size_t)g * G * DH + 2 * pr) = make_float2(acc[k].x * inv, acc[k].y * inv);
+    for (int k = 0; k < LPT; ++k) {
+      const int i = base + tid + k * NCT;
+      if (i < S * w) rv[k] = __ldcg(p.part_o + ((size_t)kh * p.smax + i / w) * E + e0 + i % w);
     }
+    const int im = r * NCT + tid;  // (m, l) pairs: one per thread and round
+    if (im < S * G) rml = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + (size_t)kh * p.smax * G + im);
+#pragma unroll
+    for (int k = 0; k < LPT; ++k) {
+      const int i = base + tid + k * NCT;
+      if (i < S * w) mo[i] = rv[k];
+    }
+    if (im < S * G) {
+      mw[im] = rml.x;
+      ml[im] = rml.y;
+    }
+  }
+  consumer_sync();
+  if (warp < G) {  // warp h: the weights of query head h, lane per piece
+    const int h = warp;
+    float mx = -INFINITY;
+    for (int q = lane; q < S; q += 32) mx = fmaxf(mx, mw[q * G + h]);
+    mx = warp_max(mx);
+    float den = 0.f;
+    for (int q = lane; q < S; q += 32) den = fmaf(expf(mw[q * G + h] - mx), ml[q * G + h], den);
+    den = warp_sum(den);
+    const float inv = 1.0f / den;
+    for (int q = lane; q < S; q += 32) mw[q * G + h] = expf(mw[q * G + h] - mx) * inv;
+  }
+  consumer_sync();
+  for (int i = tid; i < w; i += NCT) {
+    const int e = e0 + i, h = e / DH;
+    float a0 = 0.f, a1 = 0.f;
+    int q = 0;
+    for (; q + 1 < S; q += 2) {
+      a0 = fmaf(mw[q * G + h], mo[q * w + i], a0);
+      a1 = fmaf(mw[(q + 1) * G + h], mo[(q + 1) * w + i], a1);
+    }
+    if (q < S) a0 = fmaf(mw[q * G + h], mo[q * w + i], a0);
+    p.o[(size_t)kh * E + e] = a0 + a1;
   }
 }
 
@@ -398,6 +400,7 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
   const int dq = p.Hq * p.dh;
   RingPos rp{0, 0u, 0};
   uint32_t gen = 0;
+  unsigned att_target = 0;  // split-KV pieces per KV head counted so far in this launch
   unsigned long long wait_ns = 0;
   bool ok = true;
   const uint64_t t_start = globaltimer();
@@ -429,13 +432,14 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
         const int S = split_pieces(p, c);
         const int C = (c + S - 1) / S;
         const int item = blockIdx.x;
+        att_target += (unsigned)S;
         if (item < p.Hkv * S) {
-          const int gk = item / S, sp = item % S;
+          const int kh = item / S, sp = item % S;
           const int j0 = min(c, sp * C), j1 = min(c, j0 + C);
           if (p.dh == 128)
-            attention_piece<4>(p, s, l, gk, sp, S, j0, j1);
+            attention_piece<4>(p, s, l, kh, sp, S, j0, j1, att_target, g);
           else
-            attention_piece<2>(p, s, l, gk, sp, S, j0, j1);
+            attention_piece<2>(p, s, l, kh, sp, S, j0, j1, att_target, g);
         }
       }
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;

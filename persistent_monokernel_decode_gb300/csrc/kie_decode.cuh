@@ -19,7 +19,7 @@ struct Ctl {
   unsigned pad1[30];
   unsigned long long amax[2];  // packed (orderable logit, ~index) argmax of the even / odd token
   unsigned pad2[28];
-  unsigned att_cnt[MAX_KV_HEADS];  // split-KV arrivals per KV head; the last arrival merges and resets
+  unsigned att_cnt[MAX_KV_HEADS];  // split-KV pieces per KV head published so far in this launch
 };
 
 // Survives across launches.

@@ -213,6 +213,27 @@ def test_long_context_split_kv(kie):
     dec.close()
 
 
+def split_kv(c: int, smax: int):
+    """The kernel's split of c attended positions into pieces: (pieces, positions per piece)."""
+    S = min(smax, -(-c // 32))
+    return S, -(-c // S)
+
+
+def test_context_with_an_empty_split_kv_piece(kie):
+    """Contexts where the split leaves the last piece of each KV head with no positions (its partial is
+    m = -inf, l = 0, o = 0): the merge must weigh it zero. The context is found from this device's CTA count."""
+    cfg = dataclasses.replace(TINY, seed=12)
+    w = synth.model_weights(cfg)
+    dec = kie.Decoder(cfg, w, max_seq=2048)
+    smax = max(1, dec.n_cta // cfg.n_kv_heads)
+    empty = [c for c in range(1, 2040) if (lambda S, C: (S - 1) * C >= c)(*split_kv(c, smax))]
+    assert empty, "no context below 2,040 leaves a piece empty on this device"
+    c = empty[0]
+    prompt = synth.tokens(12, c - 1, cfg.vocab)  # the first decode step attends over c positions
+    check_run(dec, cfg, w, prompt, 6, 2048)
+    dec.close()
+
+
 # ---- the 2B workload at full size, in the launch configuration the bench times ---------------------------
 
 @pytest.fixture(scope="module")
