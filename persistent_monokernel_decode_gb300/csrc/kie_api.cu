@@ -42,7 +42,7 @@ struct WsLayout {
 };
 
 struct Plan {
-  int n_cta, nslot, vec_floats, out_floats;
+  int n_cta, nslot, vec_floats, out_floats, out_res, out_rope;
   size_t smem;
   WeightLayout w;
   WsLayout ws;
@@ -77,9 +77,13 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   const int smax = std::max(1, n_cta / c->n_kv_heads);
   const int att = G * dh + kie::ATT_SUB * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
   pl->vec_floats = std::max(std::max(d, c->ffn_dim), std::max(dq, att));
-  pl->out_floats = std::max(std::max(max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta),
+  // row results of the widest projection, then this CTA's slices of x and h, then the token's RoPE row
+  const int rows = std::max(std::max(max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta),
                                      max_rows_per_cta(d, n_cta)),
                             std::max(max_rows_per_cta(2 * c->ffn_dim, n_cta), max_rows_per_cta(c->vocab, n_cta)));
+  pl->out_res = (int)kie::align_up((size_t)rows, 4);
+  pl->out_rope = pl->out_res + (int)kie::align_up((size_t)2 * max_rows_per_cta(d, n_cta), 4);
+  pl->out_floats = pl->out_rope + dh;
   const size_t fixed = kie::smem_bytes(0, pl->vec_floats, pl->out_floats);
   const long long room = (long long)smem_optin - (long long)fixed - 1024;
   int nslot = room > 0 ? (int)(room / (kie::SLOT_BYTES + 16)) : 0;
@@ -298,6 +302,8 @@ void fill_base(kie_ctx *ctx) {
   p.nslot = pl.nslot;
   p.vec_floats = pl.vec_floats;
   p.out_floats = pl.out_floats;
+  p.out_res = pl.out_res;
+  p.out_rope = pl.out_rope;
   p.eps = c.rms_eps;
   p.wbase = ctx->wbuf;
   p.layer_stride = (long long)pl.w.layer_stride;

@@ -36,8 +36,10 @@ __device__ inline bool grid_barrier(const DecodeParams &p, Smem &s, uint32_t &ge
     const uint64_t t0 = globaltimer();
     bool ok = s.flags[0] == 0;
     if (ok) {
-      __threadfence();  // release this CTA's writes (ordered before by the consumer_sync above)
-      if (!((int)blockIdx.x == p.skip_cta && (int)idx == p.skip_barrier)) atomicAdd(&p.ctl->bar_count, 1u);
+      // Release add, acquire polls, then the CTA barrier: together they order every write made before any
+      // CTA's arrival before every read made after this CTA leaves. Data other CTAs wrote is always read
+      // through L2 (ld.global.cg), so no stale L1 line can be hit.
+      if (!((int)blockIdx.x == p.skip_cta && (int)idx == p.skip_barrier)) red_release_gpu_add(&p.ctl->bar_count, 1u);
       const unsigned target = (idx + 1u) * (unsigned)p.n_cta;
       for (int spins = 1;; ++spins) {
         const unsigned cur = ld_acquire_gpu(&p.ctl->bar_count);
@@ -55,7 +57,6 @@ __device__ inline bool grid_barrier(const DecodeParams &p, Smem &s, uint32_t &ge
           }
         }
       }
-      __threadfence();
     }
     const uint64_t dt = globaltimer() - t0;
     wait_ns += dt;
@@ -79,7 +80,7 @@ __device__ inline void epilogue_qkv(const DecodeParams &p, const Smem &s, int l,
   const size_t plane = (size_t)p.max_seq * dh;
   __half *Kl = p.kv + (size_t)l * 2 * p.Hkv * plane;
   __half *Vl = Kl + (size_t)p.Hkv * plane;
-  const float2 *tab = p.rope + (size_t)pos * (dh / 2);
+  const float2 *tab = reinterpret_cast<const float2 *>(s.out + p.out_rope);  // RoPE row of pos, staged per token
   for (int pr = threadIdx.x; pr < (r1 - r0) / 2; pr += NCT) {
     const int r = r0 + 2 * pr;
     float a = s.out[2 * pr], b = s.out[2 * pr + 1];
@@ -279,8 +280,7 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   // count this piece in (no reply needed), then wait for the other pieces of head kh: the counter only grows
   // during a launch, and `target` is the running total of pieces up to this layer's attention step
   if (tid == 0) {
-    __threadfence();
-    atomicAdd(&p.ctl->att_cnt[kh], 1u);
+    red_release_gpu_add(&p.ctl->att_cnt[kh], 1u);
     const uint64_t t0 = globaltimer();
     bool ok = true;
     for (int spins = 1;; ++spins) {
@@ -398,6 +398,10 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
   const RowRange rg = rows_of_cta(2 * p.F, p.n_cta, blockIdx.x);
   const RowRange rl = rows_of_cta(p.V, p.n_cta, blockIdx.x);
   const int dq = p.Hq * p.dh;
+  // this CTA's rows of x and h, kept in shared memory as well as in global memory (where the other CTAs read
+  // them), so the residual adds read nothing back
+  float *const xs = s.out + p.out_res;
+  float *const hs = xs + (ro.r1 - ro.r0);
   RingPos rp{0, 0u, 0};
   uint32_t gen = 0;
   unsigned att_target = 0;  // split-KV pieces per KV head counted so far in this launch
@@ -413,9 +417,10 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
     token = token < 0 ? 0 : (token >= p.V ? p.V - 1 : token);  // ids are checked on the host; never read outside E
     if (blockIdx.x == 0 && tid == 0 && p.out_tokens) p.out_tokens[t] = predicted;
 
-    // embed: stage E[token], keep this CTA's residual slice in x
+    // embed: stage E[token], keep this CTA's residual slice in x; stage the RoPE row of pos
     float ss = stage_f16(s, p.embed + (size_t)token * p.d, p.d, true);
-    for (int i = ro.r0 + tid; i < ro.r1; i += NCT) p.x[i] = s.vec[i];
+    for (int i = ro.r0 + tid; i < ro.r1; i += NCT) p.x[i] = xs[i - ro.r0] = s.vec[i];
+    for (int i = tid; i < p.dh; i += NCT) s.out[p.out_rope + i] = __ldg(reinterpret_cast<const float *>(p.rope) + (size_t)pos * p.dh + i);
 
     for (int l = 0; l < p.L; ++l) {
       // [QKV] + RoPE + K/V append
@@ -448,7 +453,7 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       stage_f32(s, p.o, dq, false);
       consume_region(s, p.nslot, rp, ro.r1 - ro.r0, dq, 1.0f, g);
       consumer_sync();
-      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.h[ro.r0 + i] = p.x[ro.r0 + i] + s.out[i];
+      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.h[ro.r0 + i] = hs[i] = xs[i] + s.out[i];
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
       // [GU] a = silu(gate) * up
@@ -465,7 +470,7 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       stage_f32(s, p.a, p.F, false);
       consume_region(s, p.nslot, rp, ro.r1 - ro.r0, p.F, 1.0f, g);
       consumer_sync();
-      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.x[ro.r0 + i] = p.h[ro.r0 + i] + s.out[i];
+      for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.x[ro.r0 + i] = xs[i] = hs[i] + s.out[i];
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
     }
     if (!ok) break;

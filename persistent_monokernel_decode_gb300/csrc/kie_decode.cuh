@@ -33,6 +33,7 @@ enum Mode { MODE_DECODE = 0, MODE_FORCED = 1 };
 struct DecodeParams {
   int L, d, Hq, Hkv, dh, F, V, max_seq;
   int n_cta, nslot, vec_floats, out_floats;
+  int out_res, out_rope;  // floats into the row-result area: this CTA's x and h slices, the token's RoPE row
   float eps;
   // packed weights: layer l's projections start at wbase + l * layer_stride (+ off_*)
   const uint8_t *wbase;

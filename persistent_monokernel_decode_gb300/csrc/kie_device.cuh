@@ -88,6 +88,12 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
   return v;
 }
 
+// Release add at GPU scope, no reply: the thread's earlier accesses, and those ordered before them by a CTA
+// barrier, happen before the increment for any thread that observes it with an acquire load.
+__device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
