@@ -128,6 +128,8 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   constexpr int DH = DPL * 32;
   constexpr int U = DH / 8;                          // 16-byte units per K or V row
   constexpr int UPT = (ATT_SUB * U + NCT - 1) / NCT;  // units per thread per sub-chunk
+  static_assert(ATT_SUB == 32, "one lane per position of a sub-chunk");
+  static_assert(MAX_GROUP <= NCW, "one consumer warp per query head of a group");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.Hq / p.Hkv;
   float *qs = s.vec;                                   // [G][DH], pre-scaled by 1/sqrt(dh)
@@ -158,7 +160,9 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     }
   };
   // shared memory <- the registers fetched for jb; rows past the end are zero, so that the score and P.V loops
-  // below can always run over ATT_SUB positions without guards
+  // below can always run over ATT_SUB positions without guards. K rows are stored swizzled: 16-byte chunk c
+  // of row j sits at chunk c ^ (j % U), so the score loop (one lane per row, all lanes on chunk c) reads
+  // eight different bank groups per quarter warp.
   auto stash = [&](int jb) {
     const int nb = min(ATT_SUB, j1 - jb);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -167,7 +171,8 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       const int u = tid + k * NCT;
       if (u < ATT_SUB * U) {
         const bool in = u < nb * U;
-        *reinterpret_cast<uint4 *>(Ks + (size_t)u * 8) = in ? kreg[k] : zero;
+        const int row = u / U, c = u % U;
+        *reinterpret_cast<uint4 *>(Ks + (size_t)row * DH + (size_t)(c ^ (row % U)) * 8) = in ? kreg[k] : zero;
         *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = in ? vreg[k] : zero;
       }
     }
@@ -190,51 +195,34 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     stash(jb);
     consumer_sync();                               // Ks, Vs (and qs) ready; ps free
     if (jb + ATT_SUB < j1) fetch(jb + ATT_SUB);    // next sub-chunk in flight while this one is used
-    // scores: 8 lanes per position (DH/8 dims each), 4 positions per warp, reduce over the 8 lanes
-    {
-      const int jj = warp * 4 + (lane >> 3), sub = lane & 7;
-      float kf[DH / 8];
-      const uint4 *kr = reinterpret_cast<const uint4 *>(Ks + (size_t)jj * DH + sub * (DH / 8));
-#pragma unroll
-      for (int v = 0; v < DH / 64; ++v) {
-        const uint4 raw = kr[v];
-        const __half2 *h2 = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 f = __half22float2(h2[e]);
-          kf[8 * v + 2 * e] = f.x;
-          kf[8 * v + 2 * e + 1] = f.y;
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < MAX_GROUP; ++h) {
-        if (h < G) {
-          const float4 *qh = reinterpret_cast<const float4 *>(qs + h * DH + sub * (DH / 8));
-          float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-          for (int v = 0; v < DH / 32; ++v) {
-            const float4 q4 = qh[v];
-            d0 = fmaf(kf[4 * v], q4.x, d0);
-            d1 = fmaf(kf[4 * v + 1], q4.y, d1);
-            d0 = fmaf(kf[4 * v + 2], q4.z, d0);
-            d1 = fmaf(kf[4 * v + 3], q4.w, d1);
-          }
-          float d = d0 + d1;
-          d += __shfl_xor_sync(0xffffffffu, d, 1);
-          d += __shfl_xor_sync(0xffffffffu, d, 2);
-          d += __shfl_xor_sync(0xffffffffu, d, 4);
-          if (sub == 0 && jj < nb) ps[h * ATT_SUB + jj] = d;
-        }
-      }
-    }
-    consumer_sync();
-    // online softmax: warp h owns head h, lane j position j of the sub-chunk (positions past nb weigh 0)
+    // scores and the online-softmax update: warp h owns query head h, lane j position jb + j of the sub-chunk
+    // (a whole DH-long dot product per lane, no cross-lane sums); positions past nb weigh 0
     if (warp < G) {
-      const int h = warp;
-      const float sc = lane < nb ? ps[h * ATT_SUB + lane] : -INFINITY;
+      const int h = warp, jj = lane;
+      const float4 *qh = reinterpret_cast<const float4 *>(qs + h * DH);
+      const __half *kr = Ks + (size_t)jj * DH;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll 4
+      for (int c = 0; c < U; ++c) {
+        const uint4 raw = *reinterpret_cast<const uint4 *>(kr + (c ^ (jj % U)) * 8);
+        const float4 qa = qh[2 * c], qb = qh[2 * c + 1];
+        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.z));
+        const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.w));
+        a0 = fmaf(k0.x, qa.x, a0);
+        a1 = fmaf(k0.y, qa.y, a1);
+        a2 = fmaf(k1.x, qa.z, a2);
+        a3 = fmaf(k1.y, qa.w, a3);
+        a0 = fmaf(k2.x, qb.x, a0);
+        a1 = fmaf(k2.y, qb.y, a1);
+        a2 = fmaf(k3.x, qb.z, a2);
+        a3 = fmaf(k3.y, qb.w, a3);
+      }
+      const float sc = jj < nb ? (a0 + a1) + (a2 + a3) : -INFINITY;
       const float mnew = fmaxf(mrun[h], warp_max(sc));
-      const float e = lane < nb ? expf(sc - mnew) : 0.f;
-      ps[h * ATT_SUB + lane] = e;
+      const float e = jj < nb ? expf(sc - mnew) : 0.f;
+      ps[h * ATT_SUB + jj] = e;
       const float sum = warp_sum(e);
       if (lane == 0) {
         const float c = expf(mrun[h] - mnew);
