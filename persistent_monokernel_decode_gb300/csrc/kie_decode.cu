@@ -297,7 +297,7 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   const int sl = (E + S - 1) / S;
   const int e0 = min(E, sp * sl), e1 = min(E, e0 + sl), w = e1 - e0;
   if (w == 0) return;
-  float *mo = reinterpret_cast<float *>(Ks);  // [S][w] (the K/V staging area is free now)
+  float *mo = reinterpret_cast<float *>(Ks);  // [S][w] in the K half of the staging area (free now)
   constexpr int LPT = (MAX_GROUP * DH + NCT - 1) / NCT + 1;  // o loads per thread per round
   for (int r = 0; r * LPT * NCT < S * w || r * NCT < S * G; ++r) {  // one round unless S * G > NCT
     const int base = r * LPT * NCT;
@@ -333,16 +333,20 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     for (int q = lane; q < S; q += 32) mw[q * G + h] = expf(mw[q * G + h] - mx) * inv;
   }
   consumer_sync();
+  // P threads per output, each over every P-th piece, then a sum over the P partials
+  float *red = reinterpret_cast<float *>(Vs);  // [P][w]; mo ends before the V half of the staging area
+  const int P = max(1, NCT / w);
+  for (int idx = tid; idx < P * w; idx += NCT) {
+    const int i = idx % w, part = idx / w, h = (e0 + i) / DH;
+    float a = 0.f;
+    for (int q = part; q < S; q += P) a = fmaf(mw[q * G + h], mo[q * w + i], a);
+    red[idx] = a;
+  }
+  consumer_sync();
   for (int i = tid; i < w; i += NCT) {
-    const int e = e0 + i, h = e / DH;
-    float a0 = 0.f, a1 = 0.f;
-    int q = 0;
-    for (; q + 1 < S; q += 2) {
-      a0 = fmaf(mw[q * G + h], mo[q * w + i], a0);
-      a1 = fmaf(mw[(q + 1) * G + h], mo[(q + 1) * w + i], a1);
-    }
-    if (q < S) a0 = fmaf(mw[q * G + h], mo[q * w + i], a0);
-    p.o[(size_t)kh * E + e] = a0 + a1;
+    float a = 0.f;
+    for (int part = 0; part < P; ++part) a += red[part * w + i];
+    p.o[(size_t)kh * E + e0 + i] = a;
   }
 }
 
@@ -412,6 +416,20 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
 
     for (int l = 0; l < p.L; ++l) {
       // [QKV] + RoPE + K/V append
+      {  // L2 prefetch of the cached K/V rows this CTA's attention piece will read (positions before pos)
+        const int c = pos + 1, S = split_pieces(p, c), C = (c + S - 1) / S;
+        if (tid == 0 && (int)blockIdx.x < p.Hkv * S) {
+          const int kh = blockIdx.x / S, sp = blockIdx.x % S;
+          const int j0 = min(pos, sp * C), j1 = min(pos, j0 + C);
+          if (j1 > j0) {
+            const size_t plane = (size_t)p.max_seq * p.dh;
+            const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + kh) * plane + (size_t)j0 * p.dh;
+            const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + kh) * plane + (size_t)j0 * p.dh;
+            bulk_prefetch_l2(Kb, (uint32_t)((j1 - j0) * p.dh * 2));
+            bulk_prefetch_l2(Vb, (uint32_t)((j1 - j0) * p.dh * 2));
+          }
+        }
+      }
       if (l > 0) ss = stage_f32(s, p.x, p.d, true);
       consume_region(s, p.nslot, rp, rq.r1 - rq.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
       consumer_sync();

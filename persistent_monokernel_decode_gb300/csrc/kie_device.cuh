@@ -67,6 +67,11 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 }
 
 // One contiguous global -> shared bulk copy; bytes and both addresses are multiples of 16.
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned address and size); no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
                                          uint64_t policy) {
   asm volatile(
