@@ -8,6 +8,9 @@ L2 and every token streams them all, so no L2 flush is needed between steps.
 
 --impl reference times the CPU oracle (oracle/, plain C) on the host cores on a bounded sample of the same
 workload. With N > 1 (torchrun) every rank runs an independent replica: the path has no data exchange.
+
+Other modes (not the headline line): --long runs the long-context workload (prompt 8,192, 512 new tokens);
+--gemv-sweep prints one JSON line per standalone GEMV shape (GB/s, cold HBM).
 """
 from __future__ import annotations
 
@@ -33,6 +36,97 @@ def measured_peaks():
             return json.load(f), "measured"
     except OSError:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def phase_bytes(model, c):
+    """Algorithmic bytes of each phase of one layer (and of the LM head) at c attended positions."""
+    d, dh, F = model.d_model, model.head_dim, model.ffn_dim
+    return {"qkv": 2 * (model.n_heads + 2 * model.n_kv_heads) * dh * d, "att": 2 * 2 * model.n_kv_heads * dh * c,
+            "wo": 2 * d * model.n_heads * dh, "gu": 2 * 2 * F * d, "down": 2 * d * F, "lm": 2 * model.vocab * d}
+
+
+def phase_breakdown(dec, model, prompt_len, new):
+    """Per-phase time from the grid-barrier trace of the last launch (the first tokens it recorded): a phase
+    runs from the earliest departure from the previous barrier to the last arrival at its own; the release
+    latency is the gap between the last arrival at a barrier and the earliest departure from it."""
+    import numpy as np
+    per_tok = 5 * model.n_layers + 1
+    toks = min(new, 4096 // per_tok)
+    if toks < 2:
+        return None
+    arrive, wait = dec.barrier_trace(0, toks * per_tok)
+    arrive = arrive.astype(np.float64)
+    leave = arrive + wait
+    names = ["qkv", "att", "wo", "gu", "down"]
+    per = {n: [] for n in names + ["lm"]}
+    release = []
+    for k in range(1, arrive.shape[0]):
+        j = k % per_tok
+        name = "lm" if j == per_tok - 1 else names[j % 5]
+        per[name].append((arrive[k].max() - leave[k - 1].min()) / 1e3)
+        release.append((leave[k].min() - arrive[k].max()) / 1e3)
+    c_mid = prompt_len + 1 + toks // 2
+    b = phase_bytes(model, c_mid)
+    out = {"tokens": f"{toks} tokens from c = {prompt_len + 1}", "release_latency_us": float(np.median(release)),
+           "barrier_us_per_token": float(np.median(release)) * per_tok}
+    for n, v in per.items():
+        us = float(np.median(v))
+        out[n] = {"us": us, "gbs": b[n] / us / 1e3}
+    return out
+
+
+def gemv_sweep(args):
+    """y = W x for the 25 sweep shapes through kie_gemv: CUDA-event time per launch with the weights rotated
+    over enough packed copies that every launch reads cold HBM (at least 4x L2 of distinct bytes)."""
+    import torch
+
+    import persistent_monokernel_decode_gb300 as kie
+    import synth
+    from synth.configs import GEMV_SHAPES
+    kie.build()
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    peaks, peak_kind = measured_peaks()
+    for sh in GEMV_SHAPES:
+        W, x = synth.gemv_operands(sh)
+        Wd = torch.from_numpy(W.view("int16")).cuda()
+        xd = torch.from_numpy(x.view("int16")).cuda()
+        copies = max(1, -(-4 * l2 // (2 * sh.M * sh.K)))
+        packed = [kie.gemv_pack(Wd) for _ in range(copies)]
+        y = torch.empty(sh.M, dtype=torch.float32, device="cuda")
+        for i in range(args.warmup):
+            kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
+        torch.cuda.synchronize()
+        reps = max(args.steps, 2 * copies)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ts = []
+        for i in range(reps):
+            ev[i].record()
+            kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
+            ev[i + 1].record()
+        torch.cuda.synchronize()
+        ts = sorted(ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(reps))
+        t = ts[len(ts) // 2]
+        gbs = sh.bytes() / t / 1e9
+        print(json.dumps({"metric": "standalone fp16 GEMV GB/s (one launch, cold HBM)", "M": sh.M, "K": sh.K,
+                          "value": gbs, "unit": "GB/s", "us": t * 1e6, "copies": copies,
+                          "frac_of_peak": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind}), flush=True)
+        del packed, Wd, xd, y
+
+
+def profiled_traffic(workload, digest):
+    """DRAM bytes per decode launch from the committed ncu summary of this workload, if that capture was taken
+    from the same kernel sources (the summary's `source_digest` line); otherwise None."""
+    import re
+    path = os.path.join(ROOT, "profiles", f"decode_kernel_{workload}_dram.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"^source_digest:\s*([0-9a-f]+)\s*$", text, re.M)
+    t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)\s*$", text, re.M)
+    if not m or not t or m.group(1) != digest:
+        return None
+    return float(t.group(1))
 
 
 def algorithmic_bytes(model, prompt_len, n):
@@ -162,7 +256,14 @@ def main():
     ap.add_argument("--layers", type=int, default=25, help="fewer layers of the same widths (profiling cases)")
     ap.add_argument("--prompt", type=int, default=PROMPT)
     ap.add_argument("--decode", type=int, default=NEW)
+    ap.add_argument("--long", action="store_true", help="the long-context workload: prompt 8,192, 512 new tokens")
+    ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
     args = ap.parse_args()
+    if args.long:
+        args.prompt, args.decode = 8192, 512
+    if args.gemv_sweep:
+        gemv_sweep(args)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, world, rank)
@@ -180,7 +281,8 @@ def main():
     model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
     prompt_len, new = args.prompt, args.decode
     workload = WORKLOAD if (args.layers, prompt_len, new) == (25, PROMPT, NEW) else \
-        f"llama2b_L{args.layers}_p{prompt_len}_n{new}"
+        ("llama2b_p8192_n512" if (args.layers, prompt_len, new) == (25, 8192, 512) else
+         f"llama2b_L{args.layers}_p{prompt_len}_n{new}")
 
     torch.cuda.set_device(local)
     pg = None
@@ -226,6 +328,7 @@ def main():
     torch.cuda.synchronize()
     clk = clocks.stop()
     stats = dec.barrier_stats()
+    phases = phase_breakdown(dec, model, prompt_len, new)
     step_s = sum(times) / len(times)
     if pg:
         t = torch.tensor([step_s], device="cuda", dtype=torch.float64)
@@ -266,13 +369,14 @@ def main():
                 "timed": f"reset + prefill({prompt_len}-token host prompt) + decode({new} -> host array), wall clock"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(workload, kie.source_digest()),
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": bytes_launch},
         "mbu": {"measured_peak": achieved / peaks["hbm_gbs"], "spec_8tbs": achieved / 8000.0},
         "barriers": {"per_token": stats["barriers"] / new, "mean_latency_ns": stats["mean_latency_ns"],
                      "mean_wait_ns": stats["mean_wait_ns"],
                      "wait_us_per_token": stats["mean_wait_ns"] * stats["barriers"] / new / 1e3},
+        "phases": phases,
         "clocks": clk,
     }
     dec.close()

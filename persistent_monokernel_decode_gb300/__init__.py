@@ -55,6 +55,20 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in deps)
 
 
+def source_digest() -> str:
+    """First 16 hex digits of a SHA-256 over the CUDA sources and the C header (names and contents): it
+    identifies the kernel build that a stored profile was taken from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(SOURCES + HEADERS):
+        h.update(f.encode())
+        with open(os.path.join(_CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    with open(os.path.join(_INCLUDE, "kie.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def build(force: bool = False) -> str:
     """Compile libkie.so in-tree for sm_103a (three translation units in parallel, then link)."""
     if not force and not _stale():
