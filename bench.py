@@ -76,8 +76,9 @@ def phase_breakdown(dec, model, prompt_len, new):
 
 
 def gemv_sweep(args):
-    """y = W x for the 25 sweep shapes through kie_gemv: CUDA-event time per launch with the weights rotated
-    over enough packed copies that every launch reads cold HBM (at least 4x L2 of distinct bytes)."""
+    """y = W x for the 25 sweep shapes through kie_gemv. The launches are captured in a CUDA graph (so the
+    host-side cost of each call is not timed) that cycles over enough packed copies of W that every launch
+    reads cold HBM (at least 4x L2 of distinct bytes); time per launch = replay time / launches."""
     import torch
 
     import persistent_monokernel_decode_gb300 as kie
@@ -86,6 +87,7 @@ def gemv_sweep(args):
     kie.build()
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     peaks, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
     for sh in GEMV_SHAPES:
         W, x = synth.gemv_operands(sh)
         Wd = torch.from_numpy(W.view("int16")).cuda()
@@ -93,24 +95,30 @@ def gemv_sweep(args):
         copies = max(1, -(-4 * l2 // (2 * sh.M * sh.K)))
         packed = [kie.gemv_pack(Wd) for _ in range(copies)]
         y = torch.empty(sh.M, dtype=torch.float32, device="cuda")
-        for i in range(args.warmup):
-            kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
+        per_graph = max(copies, 16)
         torch.cuda.synchronize()
-        reps = max(args.steps, 2 * copies)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-        ts = []
-        for i in range(reps):
-            ev[i].record()
-            kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
-            ev[i + 1].record()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                for i in range(per_graph):
+                    kie.gemv(packed[i % copies], xd, sh.M, sh.K, y=y)
+            g.replay()
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(stream)
         torch.cuda.synchronize()
-        ts = sorted(ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(reps))
-        t = ts[len(ts) // 2]
+        t = e0.elapsed_time(e1) / 1e3 / (args.steps * per_graph)
         gbs = sh.bytes() / t / 1e9
-        print(json.dumps({"metric": "standalone fp16 GEMV GB/s (one launch, cold HBM)", "M": sh.M, "K": sh.K,
-                          "value": gbs, "unit": "GB/s", "us": t * 1e6, "copies": copies,
+        print(json.dumps({"metric": "standalone fp16 GEMV GB/s (one launch each, cold HBM, CUDA graph)",
+                          "M": sh.M, "K": sh.K, "value": gbs, "unit": "GB/s", "us": t * 1e6, "copies": copies,
                           "frac_of_peak": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind}), flush=True)
-        del packed, Wd, xd, y
+        del g, packed, Wd, xd, y
 
 
 def profiled_traffic(workload, digest):
@@ -225,18 +233,19 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_sample(seconds_budget=20.0):
-    """The oracle as it stands on the host cores: greedy decode forwards of the 2B model (bounded)."""
+def cpu_baseline_sample(seconds_budget=15.0, max_forwards=400):
+    """The oracle as it stands on the host cores: greedy decode forwards of the 2B model, for about
+    seconds_budget of CPU time (at most max_forwards)."""
     import oracle
     import synth
     from synth.configs import TWO_B
 
     w = synth.model_weights(TWO_B)
     prompt = synth.tokens(TWO_B.seed, 8, TWO_B.vocab)
-    m = oracle.Model(TWO_B, w, 64, 32)
+    m = oracle.Model(TWO_B, w, len(prompt) + max_forwards + 1, 32)
     cur = m.prefill(prompt)
     n, t0 = 0, time.perf_counter()
-    while n < 40:
+    while n < max_forwards:
         cur = m.forward(oracle.argmax(cur))
         n += 1
         if time.perf_counter() - t0 > seconds_budget:
