@@ -20,8 +20,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_ROOT, "_build")
 LIB_PATH = os.path.join(_HERE, "libkie.so")
-SOURCES = ("kie_api.cu", "kie_decode.cu", "kie_gemv.cu")
-HEADERS = ("kie_layout.h", "kie_device.cuh", "kie_decode.cuh")
+SOURCES = ("kie_api.cu", "kie_decode.cu", "kie_gemv.cu", "kie_prefill.cu")
+HEADERS = ("kie_layout.h", "kie_device.cuh", "kie_decode.cuh", "kie_prefill.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KIE_OK, KIE_ERR_INVALID, KIE_ERR_OOM, KIE_ERR_CAPACITY = 0, -1, -2, -3
@@ -70,7 +70,7 @@ def source_digest() -> str:
 
 
 def build(force: bool = False) -> str:
-    """Compile libkie.so in-tree for sm_103a (three translation units in parallel, then link)."""
+    """Compile libkie.so in-tree for sm_103a (the translation units in parallel, then link)."""
     if not force and not _stale():
         return LIB_PATH
     os.makedirs(_BUILD, exist_ok=True)

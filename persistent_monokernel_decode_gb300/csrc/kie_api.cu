@@ -12,6 +12,7 @@
 
 #include "kie.h"
 #include "kie_decode.cuh"
+#include "kie_prefill.cuh"
 #include "kie_device.cuh"
 
 cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream);
@@ -37,7 +38,7 @@ struct WeightLayout {
 
 struct WsLayout {
   size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
-      total;
+      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, total;
   int smax;
 };
 
@@ -130,6 +131,13 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   s.tok_in = take((size_t)c->max_seq * 4);
   s.tok_out = take((size_t)c->max_seq * 4);
   s.chunk = take((size_t)LOGIT_CHUNK * c->vocab * 4);
+  // batched prefill: fp32 activations of one chunk of prompt tokens
+  s.pf_x = take((size_t)kie::PF_TOKENS * d * 4);
+  s.pf_h = take((size_t)kie::PF_TOKENS * d * 4);
+  s.pf_q = take((size_t)kie::PF_TOKENS * dq * 4);
+  s.pf_o = take((size_t)kie::PF_TOKENS * dq * 4);
+  s.pf_a = take((size_t)kie::PF_TOKENS * c->ffn_dim * 4);
+  s.pf_scale = take((size_t)kie::PF_TOKENS * 4);
   s.total = o;
   return nullptr;
 }
@@ -488,10 +496,17 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
   std::memcpy(ctx->pinned, tokens, (size_t)n * 4);
   int *tin = (int *)(ctx->wsbuf + ctx->plan.ws.tok_in);
   KIE_CUDA(ctx, cudaMemcpyAsync(tin, ctx->pinned, (size_t)n * 4, cudaMemcpyHostToDevice, ctx->stream));
-  int rc = launch(ctx, n, kie::MODE_FORCED, 1, tin, nullptr, nullptr);
-  if (rc == KIE_OK) rc = finish(ctx);
-  if (rc == KIE_OK) ctx->has_logits = true;
-  return rc;
+  // batched: the prompt moves through each layer in chunks of up to PF_TOKENS tokens (kie_prefill.cu)
+  const WsLayout &ws = ctx->plan.ws;
+  uint8_t *b = ctx->wsbuf;
+  const kie::PrefillBufs pb{(float *)(b + ws.pf_x), (float *)(b + ws.pf_h), (float *)(b + ws.pf_q),
+                            (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale)};
+  const cudaError_t e = kie_run_prefill(ctx->base, pb, tin, ctx->pos, n, ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
+  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+  ctx->pos += n;
+  ctx->has_logits = true;
+  return KIE_OK;
 }
 
 int kie_decode_async(kie_ctx *ctx, int n, int32_t *out_tokens_dev) {

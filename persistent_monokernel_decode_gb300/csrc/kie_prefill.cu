@@ -1,0 +1,456 @@
+// Batched prefill: a prompt's tokens go through each layer together, in chunks of up to PF_TOKENS, so every
+// weight is read once per chunk instead of once per token. Same arithmetic as the decode kernel (fp16 weights
+// with the RMSNorm gains folded, fp32 activations and accumulation, RoPE from the fp32 table, fp16 K/V cache,
+// max-subtracted softmax), on the same packed weights; the prompt is part of the decode problem (the pages' 2B
+// workload has a 4,096-token sequence), not a different model path.
+//
+// Kernels, per chunk of T tokens:
+//   pf_embed  X[t] = fp32(E[tok[t]])
+//   per layer: pf_rms(X) -> pf_gemm QKV (RoPE, K/V append, q) -> pf_attn (causal, over the cache) ->
+//              pf_gemm WO (H = X + Wo o) -> pf_rms(H) -> pf_gemm GU (A = silu(g) u) -> pf_gemm DOWN (X = H + Wd a)
+//   after the last chunk: pf_rms(last X) -> pf_gemm LM head (one token) -> pf_argmax (next token)
+// Every output's sums run in a fixed order that does not depend on how the prompt is cut into chunks, so a
+// prompt prefilled in pieces leaves bit-identical logits and cache.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kie_decode.cuh"
+#include "kie_layout.h"
+#include "kie_prefill.cuh"
+
+namespace kie {
+namespace {
+
+constexpr int PF_THREADS = 256;
+constexpr int PA_WARPS = 4;  // tokens (one warp each) per attention block
+constexpr int GR = TILE_ROWS;    // output rows per block pass (a row group of the packed layout)
+constexpr int KC = 32;           // columns per shared-memory stage
+constexpr int XS = PF_TOKENS + 4;  // padded token stride of the staged input (bank spread)
+
+enum Epi { EPI_QKV = 0, EPI_WO = 1, EPI_GU = 2, EPI_DOWN = 3, EPI_LM = 4 };
+
+struct GemmArgs {
+  const uint8_t *w;      // packed projection [M, K] (all CTAs' regions)
+  int M, K, n_cta;       // rows, columns, CTAs the layout was packed for
+  const float *in;       // [T][K] token-major input rows
+  const float *scale;    // [T] per-token RMS scale, or null (1)
+  int T;
+  // epilogues
+  float *out;            // WO/DOWN: [T][M]; GU: [T][M/2]; QKV: q [T][Hq*dh]; LM: [M]
+  const float *resid;    // WO/DOWN: [T][M]
+  __half *kv;            // QKV: this layer's K plane base ([2][Hkv][max_seq][dh])
+  const float2 *rope;    // QKV: [max_seq][dh/2]
+  int pos0, Hq, Hkv, dh, max_seq;
+};
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// out rows of row group blockIdx.y of CTA region blockIdx.x (rows [r0, r1) of the decode's row split), for
+// T <= PF_TOKENS tokens. Thread (ty, tx) owns rows 4ty .. 4ty+3 of the group and tokens 4tx .. 4tx+3; every
+// output is one fp32 FMA chain over k in ascending order.
+template <int EPI>
+__global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
+  __shared__ __align__(16) float Ws[KC][GR];       // W chunk, transposed: [k][row]
+  __shared__ __align__(16) float Xs[KC][XS];       // input chunk, transposed: [k][token]
+  const int tid = threadIdx.x, ty = tid >> 5, tx = tid & 31;
+  const RowRange rr = rows_of_cta(a.M, a.n_cta, blockIdx.x);
+  const int R = rr.r1 - rr.r0, K = a.K;
+  const __half *region = reinterpret_cast<const __half *>(a.w) + (size_t)rr.r0 * K;
+  {
+    const int g0 = blockIdx.y * GR;
+    if (g0 >= R) return;
+    const int rows = min(GR, R - g0);
+    const int bw = TILE_COLS;  // the packed layout's column blocks
+    const __half *gbase = region + (size_t)g0 * K;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    // 32-column stages over k = 0 .. K in order; the next stage's W and input values are loaded into registers
+    // while this stage's products run (the packed tile of column kcol is the one of block kcol / bw)
+    float f[4];
+    float4 v[PF_TOKENS * KC / 4 / PF_THREADS];
+    auto load = [&](int kcol) {
+      const int b0 = kcol / bw * bw, w = min(bw, K - b0), kc = kcol - b0;
+      const __half *tile = gbase + (size_t)rows * b0;  // [rows][w] row-major
+      const int r = tid >> 3, c = (tid & 7) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f[e] = 0.f;
+      if (r < rows && kc + c < w) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(tile + (size_t)r * w + kc + c);
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        f[0] = lo.x;
+        f[1] = lo.y;
+        f[2] = hi.x;
+        f[3] = hi.y;
+      }
+#pragma unroll
+      for (int i = 0; i < PF_TOKENS * KC / 4 / PF_THREADS; ++i) {
+        const int idx = tid + i * PF_THREADS, t = idx >> 3, cc = (idx & 7) * 4;
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < a.T && kc + cc < w) v[i] = *reinterpret_cast<const float4 *>(a.in + (size_t)t * K + kcol + cc);
+      }
+    };
+    load(0);
+    for (int kcol = 0; kcol < K; kcol += KC) {
+      {
+        const int r = tid >> 3, c = (tid & 7) * 4;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Ws[c + e][r] = f[e];
+#pragma unroll
+        for (int i = 0; i < PF_TOKENS * KC / 4 / PF_THREADS; ++i) {
+          const int idx = tid + i * PF_THREADS, t = idx >> 3, cc = (idx & 7) * 4;
+          Xs[cc][t] = v[i].x;
+          Xs[cc + 1][t] = v[i].y;
+          Xs[cc + 2][t] = v[i].z;
+          Xs[cc + 3][t] = v[i].w;
+        }
+      }
+      __syncthreads();
+      if (kcol + KC < K) load(kcol + KC);
+#pragma unroll 8
+      for (int k = 0; k < KC; ++k) {
+        const float4 wv = *reinterpret_cast<const float4 *>(&Ws[k][4 * ty]);
+        const float4 xv = *reinterpret_cast<const float4 *>(&Xs[k][4 * tx]);
+        const float wr[4] = {wv.x, wv.y, wv.z, wv.w}, xr[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) acc[i][jj] = fmaf(wr[i], xr[jj], acc[i][jj]);
+      }
+      __syncthreads();
+    }
+    // epilogue: rows g0 + 4ty + i (< R), tokens 4tx + j (< T)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int t = 4 * tx + j;
+      if (t >= a.T) continue;
+      const float sc = a.scale ? a.scale[t] : 1.0f;
+      if (EPI == EPI_QKV || EPI == EPI_GU) {
+        // rows come in adjacent pairs (RoPE halves; gate/up): handled pairwise
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+          const int lr = g0 + 4 * ty + i;
+          if (lr >= R) continue;  // R and the group start are even: the pair (lr, lr + 1) is whole
+          const int r = rr.r0 + lr;
+          const float y0 = acc[i][j] * sc, y1 = acc[i + 1][j] * sc;
+          if (EPI == EPI_GU) {
+            a.out[(size_t)t * (a.M / 2) + r / 2] = silu_mul(y0, y1);
+          } else {
+            const int dh = a.dh, qrows = a.Hq * dh, krows = a.Hkv * dh, pos = a.pos0 + t;
+            const size_t plane = (size_t)a.max_seq * dh;
+            if (r < qrows + krows) {
+              const int rq = r < qrows ? r : r - qrows;
+              const float2 cs = a.rope[(size_t)pos * (dh / 2) + (rq % dh) / 2];
+              const float a2 = y0 * cs.x - y1 * cs.y, b2 = y1 * cs.x + y0 * cs.y;
+              if (r < qrows) {
+                *reinterpret_cast<float2 *>(a.out + (size_t)t * qrows + r) = make_float2(a2, b2);
+              } else {
+                *reinterpret_cast<__half2 *>(a.kv + (size_t)(rq / dh) * plane + (size_t)pos * dh + rq % dh) =
+                    __floats2half2_rn(a2, b2);
+              }
+            } else {
+              const int rv = r - qrows - krows;
+              *reinterpret_cast<__half2 *>(a.kv + (size_t)a.Hkv * plane + (size_t)(rv / dh) * plane +
+                                           (size_t)pos * dh + rv % dh) = __floats2half2_rn(y0, y1);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int lr = g0 + 4 * ty + i;
+          if (lr >= R) continue;
+          const int r = rr.r0 + lr;
+          const float y = acc[i][j] * sc;
+          if (EPI == EPI_LM) a.out[r] = y;
+          else a.out[(size_t)t * a.M + r] = a.resid[(size_t)t * a.M + r] + y;
+        }
+      }
+    }
+  }
+}
+
+// scale[t] = 1 / sqrt(mean(x_t^2) + eps), one warp per token, lane-strided sums then a fixed tree.
+__global__ void pf_rms(const float *x, int T, int d, float eps, float *scale) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= T) return;
+  const float *row = x + (size_t)warp * d;
+  float s = 0.f;
+  for (int i = lane; i < d; i += 32) s = fmaf(row[i], row[i], s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) scale[warp] = 1.0f / sqrtf(s / (float)d + eps);
+}
+
+__global__ void pf_embed(const int *tok, int T, const __half *E, int d, float *x) {
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  const __half *row = E + (size_t)tok[t] * d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) x[(size_t)t * d + i] = __half2float(row[i]);
+}
+
+// Causal attention of T new tokens (positions pos0 .. pos0+T-1) over the cache of one layer. Block: one KV head
+// and PA_WARPS consecutive tokens, a warp per token with all G query heads of the group; the 32-position K/V
+// tiles are shared by the block. Scores, online softmax and P.V follow the decode kernel's formulas.
+template <int DPL>
+__global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, int pos0, const __half *kvl, int Hq,
+                                                         int Hkv, int max_seq, float *o) {
+  constexpr int DH = DPL * 32, U = DH / 8;
+  __shared__ __align__(16) __half Ks[32 * DH];
+  __shared__ __align__(16) __half Vs[32 * DH];
+  __shared__ __align__(16) float qs[PA_WARPS][MAX_GROUP][DH];
+  __shared__ float ps[PA_WARPS][MAX_GROUP][32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kh = blockIdx.x, G = Hq / Hkv;
+  const int t = blockIdx.y * PA_WARPS + warp;
+  const bool live = t < T;
+  const int pos = pos0 + t;  // this warp's query position
+  const int last = pos0 + min(T, blockIdx.y * PA_WARPS + PA_WARPS) - 1;  // the block's largest position
+  const size_t plane = (size_t)max_seq * DH;
+  const __half *Kb = kvl + (size_t)kh * plane, *Vb = kvl + (size_t)(Hkv + kh) * plane;
+  const float qscale = 1.0f / sqrtf((float)DH);
+  if (live)
+    for (int i = lane; i < G * DH; i += 32) qs[warp][i / DH][i % DH] = q[(size_t)t * Hq * DH + (size_t)kh * G * DH + i] * qscale;
+  float m[MAX_GROUP], l[MAX_GROUP], acc[MAX_GROUP][DPL];
+#pragma unroll
+  for (int h = 0; h < MAX_GROUP; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
+  }
+  constexpr int UPT = 32 * U / (PA_WARPS * 32);  // 16-byte units of a K (or V) tile per thread
+  static_assert(32 * U % (PA_WARPS * 32) == 0, "tile units split evenly over the block");
+  uint4 kreg[UPT], vreg[UPT];
+  auto fetch = [&](int jb) {  // registers <- K, V rows [jb, jb + 32) that exist (zeros past `last`)
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      const int u = tid + k * PA_WARPS * 32, row = u / U, c = u % U, j = jb + row;
+      kreg[k] = make_uint4(0u, 0u, 0u, 0u);
+      vreg[k] = kreg[k];
+      if (j <= last) {
+        kreg[k] = *reinterpret_cast<const uint4 *>(Kb + (size_t)j * DH + c * 8);
+        vreg[k] = *reinterpret_cast<const uint4 *>(Vb + (size_t)j * DH + c * 8);
+      }
+    }
+  };
+  fetch(0);
+  for (int jb = 0; jb <= last; jb += 32) {
+    __syncthreads();  // the previous tile is no longer read
+#pragma unroll
+    for (int k = 0; k < UPT; ++k) {
+      const int u = tid + k * PA_WARPS * 32, row = u / U, c = u % U;
+      *reinterpret_cast<uint4 *>(Ks + (size_t)row * DH + (size_t)(c ^ (row % U)) * 8) = kreg[k];
+      *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = vreg[k];
+    }
+    __syncthreads();
+    if (jb + 32 <= last) fetch(jb + 32);  // the next tile is in flight while this one is used
+    if (!live || jb > pos) continue;
+    const int j = jb + lane;
+    const bool valid = j <= pos;
+    const __half *kr = Ks + (size_t)lane * DH;
+    float s[MAX_GROUP];
+#pragma unroll
+    for (int h = 0; h < MAX_GROUP; ++h) s[h] = 0.f;
+    for (int c = 0; c < U; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(kr + (c ^ (lane % U)) * 8);
+      const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+      const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+      const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.z));
+      const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.w));
+#pragma unroll
+      for (int h = 0; h < MAX_GROUP; ++h) {
+        if (h < G) {
+          const float4 qa = *reinterpret_cast<const float4 *>(&qs[warp][h][8 * c]);
+          const float4 qb = *reinterpret_cast<const float4 *>(&qs[warp][h][8 * c + 4]);
+          float v = s[h];
+          v = fmaf(k0.x, qa.x, v);
+          v = fmaf(k0.y, qa.y, v);
+          v = fmaf(k1.x, qa.z, v);
+          v = fmaf(k1.y, qa.w, v);
+          v = fmaf(k2.x, qb.x, v);
+          v = fmaf(k2.y, qb.y, v);
+          v = fmaf(k3.x, qb.z, v);
+          v = fmaf(k3.y, qb.w, v);
+          s[h] = v;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < MAX_GROUP; ++h) {
+      if (h < G) {
+        const float sc = valid ? s[h] : -INFINITY;
+        float mx = sc;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float mnew = fmaxf(m[h], mx);
+        const float e = valid ? expf(sc - mnew) : 0.f;
+        ps[warp][h][lane] = e;
+        float sum = e;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        const float corr = expf(m[h] - mnew);
+        l[h] = l[h] * corr + sum;
+        m[h] = mnew;
+#pragma unroll
+        for (int e2 = 0; e2 < DPL; ++e2) acc[h][e2] *= corr;
+      }
+    }
+    __syncwarp();
+    // P.V: lane owns dims lane*DPL .. +DPL
+    for (int jj = 0; jj < 32; ++jj) {
+      float v[DPL];
+      if (DPL == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(Vs + (size_t)jj * DH + lane * 4);
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+        const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+        v[0] = a0.x;
+        v[1] = a0.y;
+        v[2 % DPL] = a1.x;
+        v[3 % DPL] = a1.y;
+      } else {
+        const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(Vs + (size_t)jj * DH + lane * 2));
+        v[0] = a0.x;
+        v[1 % DPL] = a0.y;
+      }
+#pragma unroll
+      for (int h = 0; h < MAX_GROUP; ++h)
+        if (h < G) {
+          const float pj = ps[warp][h][jj];
+#pragma unroll
+          for (int e2 = 0; e2 < DPL; ++e2) acc[h][e2] = fmaf(pj, v[e2], acc[h][e2]);
+        }
+    }
+    __syncwarp();
+  }
+  if (!live) return;
+#pragma unroll
+  for (int h = 0; h < MAX_GROUP; ++h)
+    if (h < G) {
+      const float inv = 1.0f / l[h];
+#pragma unroll
+      for (int e2 = 0; e2 < DPL; ++e2)
+        o[(size_t)t * Hq * DH + (size_t)(kh * G + h) * DH + lane * DPL + e2] = acc[h][e2] * inv;
+    }
+}
+
+// argmax over the logits (lowest index on ties), written as the next token to emit.
+__global__ void pf_argmax(const float *logits, int V, Persist *persist) {
+  __shared__ unsigned long long best[32];
+  unsigned long long b = 0ull;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    const unsigned u = __float_as_uint(logits[i]);
+    const unsigned ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    const unsigned long long key = ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)i);
+    b = key > b ? key : b;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+    b = other > b ? other : b;
+  }
+  if ((threadIdx.x & 31) == 0) best[threadIdx.x >> 5] = b;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = best[w] > m ? best[w] : m;
+    persist->next_token = (int)(0xFFFFFFFFu - (unsigned)(m & 0xFFFFFFFFull));
+  }
+}
+
+template <int EPI>
+cudaError_t gemm(const GemmArgs &a, cudaStream_t st) {
+  const int groups = (2 * ((a.M / 2 + a.n_cta - 1) / a.n_cta) + GR - 1) / GR;  // row groups of the largest region
+  pf_gemm<EPI><<<dim3(a.n_cta, groups), PF_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace kie
+
+cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &b, const int *tok_dev, int pos0,
+                            int n, cudaStream_t st) {
+  using namespace kie;
+  const int d = p.d, dq = p.Hq * p.dh, F = p.F, qkv = (p.Hq + 2 * p.Hkv) * p.dh;
+  const size_t plane = (size_t)p.max_seq * p.dh;
+  cudaError_t e = cudaSuccess;
+  int last_t = 0;
+  for (int c0 = 0; c0 < n; c0 += PF_TOKENS) {
+    const int T = n - c0 < PF_TOKENS ? n - c0 : PF_TOKENS, pos = pos0 + c0;
+    last_t = T - 1;
+    pf_embed<<<T, 256, 0, st>>>(tok_dev + c0, T, p.embed, d, b.x);
+    const int rms_blocks = (T * 32 + 255) / 256;
+    for (int l = 0; l < p.L; ++l) {
+      const uint8_t *lw = p.wbase + (size_t)l * p.layer_stride;
+      __half *kvl = p.kv + (size_t)l * 2 * p.Hkv * plane;
+      pf_rms<<<rms_blocks, 256, 0, st>>>(b.x, T, d, p.eps, b.scale);
+      GemmArgs a{};
+      a.n_cta = p.n_cta;
+      a.T = T;
+      a.pos0 = pos;
+      a.Hq = p.Hq;
+      a.Hkv = p.Hkv;
+      a.dh = p.dh;
+      a.max_seq = p.max_seq;
+      a.rope = p.rope;
+      a.kv = kvl;
+      // QKV (+ RoPE, K/V append, q)
+      a.w = lw + p.off_qkv;
+      a.M = qkv;
+      a.K = d;
+      a.in = b.x;
+      a.scale = b.scale;
+      a.out = b.q;
+      if ((e = gemm<EPI_QKV>(a, st)) != cudaSuccess) return e;
+      // attention over positions 0 .. pos0 + t
+      const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS);
+      if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
+      else pf_attn<2><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
+      // WO + residual
+      a.w = lw + p.off_wo;
+      a.M = d;
+      a.K = dq;
+      a.in = b.o;
+      a.scale = nullptr;
+      a.out = b.h;
+      a.resid = b.x;
+      if ((e = gemm<EPI_WO>(a, st)) != cudaSuccess) return e;
+      // gate/up + SwiGLU
+      pf_rms<<<rms_blocks, 256, 0, st>>>(b.h, T, d, p.eps, b.scale);
+      a.w = lw + p.off_gu;
+      a.M = 2 * F;
+      a.K = d;
+      a.in = b.h;
+      a.scale = b.scale;
+      a.out = b.a;
+      if ((e = gemm<EPI_GU>(a, st)) != cudaSuccess) return e;
+      // down + residual
+      a.w = lw + p.off_down;
+      a.M = d;
+      a.K = F;
+      a.in = b.a;
+      a.scale = nullptr;
+      a.out = b.x;
+      a.resid = b.h;
+      if ((e = gemm<EPI_DOWN>(a, st)) != cudaSuccess) return e;
+    }
+  }
+  // logits of the last prompt token and the next token to emit
+  const float *xl = b.x + (size_t)last_t * d;
+  pf_rms<<<1, 32, 0, st>>>(xl, 1, d, p.eps, b.scale);
+  kie::GemmArgs a{};
+  a.w = p.w_lm;
+  a.M = p.V;
+  a.K = d;
+  a.n_cta = p.n_cta;
+  a.in = xl;
+  a.scale = b.scale;
+  a.T = 1;
+  a.out = p.logits;
+  if ((e = kie::gemm<kie::EPI_LM>(a, st)) != cudaSuccess) return e;
+  kie::pf_argmax<<<1, 1024, 0, st>>>(p.logits, p.V, p.persist);
+  return cudaGetLastError();
+}

@@ -137,6 +137,27 @@ def test_prefill_in_pieces_equals_whole(tiny):
     np.testing.assert_array_equal(dec.logits(), a)
 
 
+def test_batched_prefill_across_chunks_is_independent_of_the_cut(kie):
+    """A 300-token prompt spans three 128-token prefill chunks; prefilled whole or in uneven pieces it must
+    leave bit-identical logits (every sum runs in an order the chunking does not change), and both must match
+    the oracle."""
+    cfg = dataclasses.replace(TINY, seed=14)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(14, 300, cfg.vocab)
+    dec = kie.Decoder(cfg, w, max_seq=320)
+    dec.reset()
+    dec.prefill(prompt)
+    whole = dec.logits()
+    dec.reset()
+    for a, b in ((0, 100), (100, 101), (101, 250), (250, 300)):
+        dec.prefill(prompt[a:b])
+    np.testing.assert_array_equal(dec.logits(), whole)
+    assert dec.position == 300
+    _, ref_logits = oracle.generate(cfg, w, prompt, 0, max_seq=320)
+    assert float(np.max(np.abs(whole - ref_logits[0]))) <= LOGIT_TOL
+    dec.close()
+
+
 def test_api_errors(tiny, kie):
     _, dec = tiny
     dec.reset()
