@@ -83,9 +83,11 @@ int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *s
                             size_t weights_bytes, void *kv_dev, size_t kv_bytes, void *workspace_dev,
                             size_t workspace_bytes, kie_ctx **out);
 
-/* Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 in one
- * launch of the monokernel in forced-token mode; keeps the logits of the last one (so the next decode can
- * start). Synchronous. Errors: INVALID (n < 1, bad id), CAPACITY, CUDA, LAUNCH, TIMEOUT. */
+/* Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 and keep the
+ * logits of the last one (so the next decode can start). The tokens go through each layer together, in chunks
+ * of up to 128 (batched GEMMs over the packed weights, causal attention over the cache): the same arithmetic
+ * as a decode step, and the result does not depend on how a prompt is split over calls. Synchronous.
+ * Errors: INVALID (n < 1, bad id), CAPACITY, CUDA. */
 int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n);
 
 /* Greedy decode of n tokens in ONE launch (the hot path). Token i is the argmax of the current logits
