@@ -10,7 +10,8 @@ L2 and every token streams them all, so no L2 flush is needed between steps.
 workload. With N > 1 (torchrun) every rank runs an independent replica: the path has no data exchange.
 
 Other modes (not the headline line): --long runs the long-context workload (prompt 8,192, 512 new tokens);
---gemv-sweep prints one JSON line per standalone GEMV shape (GB/s, cold HBM).
+--gemv-sweep prints one JSON line per standalone GEMV shape (GB/s, cold HBM); --phase-gemv does the same for
+the decode's five projection shapes of the 2B model (the phase-split view of the weight stream).
 """
 from __future__ import annotations
 
@@ -75,8 +76,8 @@ def phase_breakdown(dec, model, prompt_len, new):
     return out
 
 
-def gemv_sweep(args):
-    """y = W x for the 25 sweep shapes through kie_gemv. The launches are captured in a CUDA graph (so the
+def gemv_sweep(args, shapes=None, label="standalone fp16 GEMV GB/s (one launch each, cold HBM, CUDA graph)"):
+    """y = W x for the 25 sweep shapes (or `shapes`) through kie_gemv. The launches are captured in a CUDA graph (so the
     host-side cost of each call is not timed) that cycles over enough packed copies of W that every launch
     reads cold HBM (at least 4x L2 of distinct bytes); time per launch = replay time / launches."""
     import torch
@@ -85,10 +86,11 @@ def gemv_sweep(args):
     import synth
     from synth.configs import GEMV_SHAPES
     kie.build()
+    shapes = shapes or GEMV_SHAPES
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     peaks, peak_kind = measured_peaks()
     stream = torch.cuda.Stream()
-    for sh in GEMV_SHAPES:
+    for sh in shapes:
         W, x = synth.gemv_operands(sh)
         Wd = torch.from_numpy(W.view("int16")).cuda()
         xd = torch.from_numpy(x.view("int16")).cuda()
@@ -115,10 +117,26 @@ def gemv_sweep(args):
         torch.cuda.synchronize()
         t = e0.elapsed_time(e1) / 1e3 / (args.steps * per_graph)
         gbs = sh.bytes() / t / 1e9
-        print(json.dumps({"metric": "standalone fp16 GEMV GB/s (one launch each, cold HBM, CUDA graph)",
-                          "M": sh.M, "K": sh.K, "value": gbs, "unit": "GB/s", "us": t * 1e6, "copies": copies,
+        print(json.dumps({"metric": label, "phase": getattr(sh, "phase", None), "M": sh.M, "K": sh.K, "value": gbs, "unit": "GB/s", "us": t * 1e6, "copies": copies,
                           "frac_of_peak": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind}), flush=True)
         del g, packed, Wd, xd, y
+
+
+def phase_shapes():
+    """The decode's projections of the 2B model as standalone GEMV shapes (seeded like the sweep)."""
+    import dataclasses
+
+    from synth.configs import TWO_B, GemvShape
+
+    @dataclasses.dataclass(frozen=True)
+    class PhaseShape(GemvShape):
+        phase: str = ""
+
+    m = TWO_B
+    d, dq, F = m.d_model, m.n_heads * m.head_dim, m.ffn_dim
+    dims = [("qkv", (m.n_heads + 2 * m.n_kv_heads) * m.head_dim, d), ("wo", d, dq), ("gate_up", 2 * F, d),
+            ("down", d, F), ("lm_head", m.vocab, d)]
+    return [PhaseShape(M, K, 2000 + i, phase=name) for i, (name, M, K) in enumerate(dims)]
 
 
 def profiled_traffic(workload, digest):
@@ -267,11 +285,16 @@ def main():
     ap.add_argument("--decode", type=int, default=NEW)
     ap.add_argument("--long", action="store_true", help="the long-context workload: prompt 8,192, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
+    ap.add_argument("--phase-gemv", action="store_true",
+                    help="the decode's five projection shapes of the 2B model through the standalone GEMV (GB/s each)")
     args = ap.parse_args()
     if args.long:
         args.prompt, args.decode = 8192, 512
     if args.gemv_sweep:
         gemv_sweep(args)
+        return
+    if args.phase_gemv:
+        gemv_sweep(args, phase_shapes(), "2B decode projection as one standalone GEMV: GB/s (cold HBM, CUDA graph)")
         return
     world, rank, local = dist_setup()
     if args.impl == "reference":
