@@ -55,17 +55,20 @@ def _stale() -> bool:
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def source_digest() -> str:
-    """First 16 hex digits of a SHA-256 over the CUDA sources and the C header (names and contents): it
-    identifies the kernel build that a stored profile was taken from."""
+# The sources a decode launch is built from: the kernel, its ring and GEMV consumer, the packed layout, and the
+# host code that plans and launches it.
+DECODE_SOURCES = ("kie_decode.cu", "kie_device.cuh", "kie_decode.cuh", "kie_layout.h", "kie_api.cu")
+
+
+def source_digest(files=DECODE_SOURCES) -> str:
+    """First 16 hex digits of a SHA-256 over the named CUDA sources (names and contents), by default those of
+    the decode launch: it identifies the kernel build that a stored profile was taken from."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(SOURCES + HEADERS):
+    for f in sorted(files):
         h.update(f.encode())
         with open(os.path.join(_CSRC, f), "rb") as fh:
             h.update(fh.read())
-    with open(os.path.join(_INCLUDE, "kie.h"), "rb") as fh:
-        h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -38,7 +38,8 @@ struct WeightLayout {
 
 struct WsLayout {
   size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
-      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, total;
+      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, total;
+  int pf_part_rows;
   int smax;
 };
 
@@ -138,6 +139,8 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   s.pf_o = take((size_t)kie::PF_TOKENS * dq * 4);
   s.pf_a = take((size_t)kie::PF_TOKENS * c->ffn_dim * 4);
   s.pf_scale = take((size_t)kie::PF_TOKENS * 4);
+  s.pf_part_rows = std::max((c->n_heads + 2 * c->n_kv_heads) * dh, d);  // the projections that may be split
+  s.pf_part = take((size_t)kie::PF_PART_SLICES * kie::PF_TOKENS * s.pf_part_rows * 4);
   s.total = o;
   return nullptr;
 }
@@ -500,7 +503,8 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
   const WsLayout &ws = ctx->plan.ws;
   uint8_t *b = ctx->wsbuf;
   const kie::PrefillBufs pb{(float *)(b + ws.pf_x), (float *)(b + ws.pf_h), (float *)(b + ws.pf_q),
-                            (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale)};
+                            (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale),
+                            (float *)(b + ws.pf_part), ws.pf_part_rows};
   const cudaError_t e = kie_run_prefill(ctx->base, pb, tin, ctx->pos, n, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
   KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));

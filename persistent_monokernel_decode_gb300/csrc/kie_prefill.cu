@@ -41,9 +41,50 @@ struct GemmArgs {
   __half *kv;            // QKV: this layer's K plane base ([2][Hkv][max_seq][dh])
   const float2 *rope;    // QKV: [max_seq][dh/2]
   int pos0, Hq, Hkv, dh, max_seq;
+  // split K: ksplit blocks per row group each sum a contiguous 1/ksplit of the columns into part
+  // ([ksplit][PF_TOKENS][M] raw sums); pf_reduce then adds the slices in order and applies the epilogue
+  int ksplit;
+  float *part;
 };
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Epilogue of the row pair (r, r + 1) of token t from their raw sums s0, s1 (QKV: RoPE, then q to out or k/v
+// to the fp16 cache; GU: SwiGLU). Pairs are RoPE halves or gate/up rows, adjacent in the packed order.
+template <int EPI>
+__device__ __forceinline__ void epi_pair(const GemmArgs &a, int t, int r, float s0, float s1) {
+  const float sc = a.scale ? a.scale[t] : 1.0f;
+  const float y0 = s0 * sc, y1 = s1 * sc;
+  if (EPI == EPI_GU) {
+    a.out[(size_t)t * (a.M / 2) + r / 2] = silu_mul(y0, y1);
+  } else {
+    const int dh = a.dh, qrows = a.Hq * dh, krows = a.Hkv * dh, pos = a.pos0 + t;
+    const size_t plane = (size_t)a.max_seq * dh;
+    if (r < qrows + krows) {
+      const int rq = r < qrows ? r : r - qrows;
+      const float2 cs = a.rope[(size_t)pos * (dh / 2) + (rq % dh) / 2];
+      const float a2 = y0 * cs.x - y1 * cs.y, b2 = y1 * cs.x + y0 * cs.y;
+      if (r < qrows) {
+        *reinterpret_cast<float2 *>(a.out + (size_t)t * qrows + r) = make_float2(a2, b2);
+      } else {
+        *reinterpret_cast<__half2 *>(a.kv + (size_t)(rq / dh) * plane + (size_t)pos * dh + rq % dh) =
+            __floats2half2_rn(a2, b2);
+      }
+    } else {
+      const int rv = r - qrows - krows;
+      *reinterpret_cast<__half2 *>(a.kv + (size_t)a.Hkv * plane + (size_t)(rv / dh) * plane + (size_t)pos * dh +
+                                   rv % dh) = __floats2half2_rn(y0, y1);
+    }
+  }
+}
+
+// Epilogue of row r of token t from its raw sum s (WO/DOWN: residual add; LM: logits of the one token).
+template <int EPI>
+__device__ __forceinline__ void epi_one(const GemmArgs &a, int t, int r, float s) {
+  const float y = s * (a.scale ? a.scale[t] : 1.0f);
+  if (EPI == EPI_LM) a.out[r] = y;
+  else a.out[(size_t)t * a.M + r] = a.resid[(size_t)t * a.M + r] + y;
+}
 
 // out rows of row group blockIdx.y of CTA region blockIdx.x (rows [r0, r1) of the decode's row split), for
 // T <= PF_TOKENS tokens. Thread (ty, tx) owns rows 4ty .. 4ty+3 of the group and tokens 4tx .. 4tx+3; every
@@ -57,8 +98,9 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
   const int R = rr.r1 - rr.r0, K = a.K;
   const __half *region = reinterpret_cast<const __half *>(a.w) + (size_t)rr.r0 * K;
   {
-    const int g0 = blockIdx.y * GR;
+    const int g0 = (int)(blockIdx.y / a.ksplit) * GR, kpart = (int)(blockIdx.y % a.ksplit);
     if (g0 >= R) return;
+    const int k_lo = K / a.ksplit * kpart, k_hi = K / a.ksplit * (kpart + 1);
     const int rows = min(GR, R - g0);
     const int bw = TILE_COLS;  // the packed layout's column blocks
     const __half *gbase = region + (size_t)g0 * K;
@@ -93,8 +135,8 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
         if (t < a.T && kc + cc < w) v[i] = *reinterpret_cast<const float4 *>(a.in + (size_t)t * K + kcol + cc);
       }
     };
-    load(0);
-    for (int kcol = 0; kcol < K; kcol += KC) {
+    load(k_lo);
+    for (int kcol = k_lo; kcol < k_hi; kcol += KC) {
       {
         const int r = tid >> 3, c = (tid & 7) * 4;
 #pragma unroll
@@ -109,7 +151,7 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
         }
       }
       __syncthreads();
-      if (kcol + KC < K) load(kcol + KC);
+      if (kcol + KC < k_hi) load(kcol + KC);
 #pragma unroll 8
       for (int k = 0; k < KC; ++k) {
         const float4 wv = *reinterpret_cast<const float4 *>(&Ws[k][4 * ty]);
@@ -122,55 +164,42 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
       }
       __syncthreads();
     }
-    // epilogue: rows g0 + 4ty + i (< R), tokens 4tx + j (< T)
+    // epilogue (or the raw sums of this K slice): rows g0 + 4ty + i (< R), tokens 4tx + j (< T)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int t = 4 * tx + j;
       if (t >= a.T) continue;
-      const float sc = a.scale ? a.scale[t] : 1.0f;
-      if (EPI == EPI_QKV || EPI == EPI_GU) {
-        // rows come in adjacent pairs (RoPE halves; gate/up): handled pairwise
 #pragma unroll
-        for (int i = 0; i < 4; i += 2) {
-          const int lr = g0 + 4 * ty + i;
-          if (lr >= R) continue;  // R and the group start are even: the pair (lr, lr + 1) is whole
-          const int r = rr.r0 + lr;
-          const float y0 = acc[i][j] * sc, y1 = acc[i + 1][j] * sc;
-          if (EPI == EPI_GU) {
-            a.out[(size_t)t * (a.M / 2) + r / 2] = silu_mul(y0, y1);
-          } else {
-            const int dh = a.dh, qrows = a.Hq * dh, krows = a.Hkv * dh, pos = a.pos0 + t;
-            const size_t plane = (size_t)a.max_seq * dh;
-            if (r < qrows + krows) {
-              const int rq = r < qrows ? r : r - qrows;
-              const float2 cs = a.rope[(size_t)pos * (dh / 2) + (rq % dh) / 2];
-              const float a2 = y0 * cs.x - y1 * cs.y, b2 = y1 * cs.x + y0 * cs.y;
-              if (r < qrows) {
-                *reinterpret_cast<float2 *>(a.out + (size_t)t * qrows + r) = make_float2(a2, b2);
-              } else {
-                *reinterpret_cast<__half2 *>(a.kv + (size_t)(rq / dh) * plane + (size_t)pos * dh + rq % dh) =
-                    __floats2half2_rn(a2, b2);
-              }
-            } else {
-              const int rv = r - qrows - krows;
-              *reinterpret_cast<__half2 *>(a.kv + (size_t)a.Hkv * plane + (size_t)(rv / dh) * plane +
-                                           (size_t)pos * dh + rv % dh) = __floats2half2_rn(y0, y1);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int lr = g0 + 4 * ty + i;
-          if (lr >= R) continue;
-          const int r = rr.r0 + lr;
-          const float y = acc[i][j] * sc;
-          if (EPI == EPI_LM) a.out[r] = y;
-          else a.out[(size_t)t * a.M + r] = a.resid[(size_t)t * a.M + r] + y;
+      for (int i = 0; i < 4; ++i) {
+        const int lr = g0 + 4 * ty + i;
+        if (lr >= R) continue;
+        const int r = rr.r0 + lr;
+        if (a.ksplit > 1) {
+          a.part[((size_t)kpart * PF_TOKENS + t) * a.M + r] = acc[i][j];
+        } else if (EPI == EPI_QKV || EPI == EPI_GU) {
+          if ((i & 1) == 0) epi_pair<EPI>(a, t, r, acc[i][j], acc[i + 1][j]);  // R and g0 even: pairs whole
+        } else {
+          epi_one<EPI>(a, t, r, acc[i][j]);
         }
       }
     }
   }
+}
+
+// The split-K sums: slices added in order (a fixed order, whatever the chunking), then the epilogue.
+template <int EPI>
+__global__ void pf_reduce(const GemmArgs a) {
+  const int per_t = (EPI == EPI_QKV || EPI == EPI_GU) ? a.M / 2 : a.M;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)a.T * per_t) return;
+  const int t = (int)(idx / per_t), u = (int)(idx % per_t);
+  auto sum = [&](int r) {
+    float v = a.part[(size_t)t * a.M + r];
+    for (int k = 1; k < a.ksplit; ++k) v += a.part[((size_t)k * PF_TOKENS + t) * a.M + r];
+    return v;
+  };
+  if (EPI == EPI_QKV || EPI == EPI_GU) epi_pair<EPI>(a, t, 2 * u, sum(2 * u), sum(2 * u + 1));
+  else epi_one<EPI>(a, t, u, sum(u));
 }
 
 // scale[t] = 1 / sqrt(mean(x_t^2) + eps), one warp per token, lane-strided sums then a fixed tree.
@@ -361,10 +390,22 @@ __global__ void pf_argmax(const float *logits, int V, Persist *persist) {
   }
 }
 
+constexpr int KSPLIT_COLS = 1280;  // columns per K slice when a projection is split
+
+// One projection: blocks over (CTA region, row group, K slice). Projections whose regions are a single row
+// group (too few blocks to fill the GPU otherwise) are split into slices of KSPLIT_COLS columns.
 template <int EPI>
-cudaError_t gemm(const GemmArgs &a, cudaStream_t st) {
+cudaError_t gemm(GemmArgs a, float *part, int part_rows, cudaStream_t st) {
   const int groups = (2 * ((a.M / 2 + a.n_cta - 1) / a.n_cta) + GR - 1) / GR;  // row groups of the largest region
-  pf_gemm<EPI><<<dim3(a.n_cta, groups), PF_THREADS, 0, st>>>(a);
+  a.ksplit = 1;
+  a.part = part;
+  if (groups == 1 && part && a.M <= part_rows && a.K % KSPLIT_COLS == 0 && a.K / KSPLIT_COLS <= PF_PART_SLICES)
+    a.ksplit = a.K / KSPLIT_COLS;
+  pf_gemm<EPI><<<dim3(a.n_cta, groups * a.ksplit), PF_THREADS, 0, st>>>(a);
+  if (a.ksplit > 1) {
+    const long long n = (long long)a.T * ((EPI == EPI_QKV || EPI == EPI_GU) ? a.M / 2 : a.M);
+    pf_reduce<EPI><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
 
@@ -404,7 +445,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.in = b.x;
       a.scale = b.scale;
       a.out = b.q;
-      if ((e = gemm<EPI_QKV>(a, st)) != cudaSuccess) return e;
+      if ((e = gemm<EPI_QKV>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
       // attention over positions 0 .. pos0 + t
       const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS);
       if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
@@ -417,7 +458,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.scale = nullptr;
       a.out = b.h;
       a.resid = b.x;
-      if ((e = gemm<EPI_WO>(a, st)) != cudaSuccess) return e;
+      if ((e = gemm<EPI_WO>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
       // gate/up + SwiGLU
       pf_rms<<<rms_blocks, 256, 0, st>>>(b.h, T, d, p.eps, b.scale);
       a.w = lw + p.off_gu;
@@ -426,7 +467,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.in = b.h;
       a.scale = b.scale;
       a.out = b.a;
-      if ((e = gemm<EPI_GU>(a, st)) != cudaSuccess) return e;
+      if ((e = gemm<EPI_GU>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
       // down + residual
       a.w = lw + p.off_down;
       a.M = d;
@@ -435,7 +476,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.scale = nullptr;
       a.out = b.x;
       a.resid = b.h;
-      if ((e = gemm<EPI_DOWN>(a, st)) != cudaSuccess) return e;
+      if ((e = gemm<EPI_DOWN>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
     }
   }
   // logits of the last prompt token and the next token to emit
@@ -450,7 +491,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
   a.scale = b.scale;
   a.T = 1;
   a.out = p.logits;
-  if ((e = kie::gemm<kie::EPI_LM>(a, st)) != cudaSuccess) return e;
+  if ((e = kie::gemm<kie::EPI_LM>(a, nullptr, 0, st)) != cudaSuccess) return e;
   kie::pf_argmax<<<1, 1024, 0, st>>>(p.logits, p.V, p.persist);
   return cudaGetLastError();
 }

@@ -8,10 +8,14 @@ namespace kie {
 
 constexpr int PF_TOKENS = 128;  // prompt tokens per chunk
 
+constexpr int PF_PART_SLICES = 6;  // K slices of a split projection, at most
+
 // fp32 activations of one chunk (device): x, h [PF_TOKENS][d]; q, o [PF_TOKENS][Hq*dh]; a [PF_TOKENS][F];
-// scale [PF_TOKENS] (per-token RMS scale).
+// scale [PF_TOKENS] (per-token RMS scale); part [PF_PART_SLICES][PF_TOKENS][max rows of a split projection]
+// (partial sums of K slices).
 struct PrefillBufs {
-  float *x, *h, *q, *o, *a, *scale;
+  float *x, *h, *q, *o, *a, *scale, *part;
+  int part_rows;  // rows of part: a projection is split only if it has at most this many
 };
 
 }  // namespace kie
