@@ -203,6 +203,29 @@ class ClockSampler:
                 "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x, pg, device="cuda"):
+    """The largest x over all ranks of the process group (x itself without one): the job's time is the
+    slowest rank's."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_rank, step_s):
+    """Whole-job tokens/s of `world` independent replicas that each decode tokens_per_rank in step_s (the
+    slowest rank's step time)."""
+    return world * tokens_per_rank / step_s
+
+
+def emit(line, rank):
+    """The JSON line is printed by rank 0 only."""
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -361,12 +384,8 @@ def main():
     clk = clocks.stop()
     stats = dec.barrier_stats()
     phases = phase_breakdown(dec, model, prompt_len, new)
-    step_s = sum(times) / len(times)
-    if pg:
-        t = torch.tensor([step_s], device="cuda", dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        step_s = float(t.item())
-    value = world * new / step_s
+    step_s = max_over_ranks(sum(times) / len(times), pg)
+    value = replica_throughput(world, new, step_s)
 
     # end to end through the host-buffer API: reset + prefill(host prompt) + decode(n, host tokens)
     e2e_times = []
@@ -380,11 +399,7 @@ def main():
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             e2e_times.append(dt)
-    e2e_step = sum(e2e_times) / len(e2e_times)
-    if pg:
-        t = torch.tensor([e2e_step], device="cuda", dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_step = float(t.item())
+    e2e_step = max_over_ranks(sum(e2e_times) / len(e2e_times), pg)
 
     peaks, peak_kind = measured_peaks()
     bytes_launch = algorithmic_bytes(model, prompt_len, new)
@@ -396,7 +411,7 @@ def main():
         "config": {"workload": workload, "prompt": prompt_len, "decode_tokens": new, "weights": "fp16",
                    "kv_cache": "fp16", "l2": "no flush: 3.9 GB of weights (> 129 MB L2) streamed per token",
                    "parallelism": "replicas" if world > 1 else "single GPU", "n_cta": dec.n_cta},
-        "e2e": {"value": world * new / e2e_step, "unit": "tok/s", "h2d_bytes_per_step": prompt_len * 4,
+        "e2e": {"value": replica_throughput(world, new, e2e_step), "unit": "tok/s", "h2d_bytes_per_step": prompt_len * 4,
                 "d2h_bytes_per_step": new * 4 + 8,
                 "timed": f"reset + prefill({prompt_len}-token host prompt) + decode({new} -> host array), wall clock"},
         "gpu_launches": args.steps,
@@ -414,8 +429,7 @@ def main():
     dec.close()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    emit(line, rank)
     if pg:
         pg.destroy_process_group()
 
