@@ -41,6 +41,11 @@ def build(force: bool = False) -> None:
         subprocess.check_call(build_cmd())
 
 
+class OrcMoe(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int), ("top_k", ctypes.c_int), ("expert_ffn", ctypes.c_int)] + \
+        [(n, P) for n in ("router", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s")]
+
+
 def lib():
     global _lib
     if _lib is None:
@@ -59,6 +64,10 @@ def lib():
             "orc_create": ([ctypes.POINTER(OrcConfig), ctypes.POINTER(OrcWeights), i], P),
             "orc_destroy": ([P], None), "orc_pos": ([P], i), "orc_reset": ([P], None),
             "orc_forward": ([P, i, P], i), "orc_kv_row": ([P, i, i, i, i, P], None),
+            "orc_set_moe": ([P, ctypes.POINTER(OrcMoe)], i), "orc_moe_ffn": ([P, i, P, P], None),
+            "orc_e4m3_to_double": ([ctypes.c_uint8], d),
+            "orc_gemv_fp8_f32": ([P, P, P, i, i, P], None), "orc_gemv_fp8_f64": ([P, P, P, i, i, P], None),
+            "orc_topk_softmax_f64": ([P, i, i, P, P], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -129,6 +138,30 @@ def attention(q, K_bits, V_bits, precision=32):
     return out
 
 
+def e4m3_to_double(code: int) -> float:
+    return lib().orc_e4m3_to_double(code)
+
+
+def gemv_fp8(q, scale, x, precision=64):
+    """y = diag(scale) E4M3(q) x for codes q [M, K] (uint8) and row scales [M] (float32)."""
+    q, pq = _c(q, np.uint8)
+    sc, ps = _c(scale, np.float32)
+    x, px = _c(x, _real(precision))
+    M, K = q.shape
+    y = np.empty(M, dtype=_real(precision))
+    getattr(lib(), f"orc_gemv_fp8_f{precision}")(pq, ps, px, M, K, y.ctypes.data)
+    return y
+
+
+def topk_softmax(r, k):
+    """(indices of the k largest of r, lowest index first on ties, in descending order; softmax over them)."""
+    r, pr = _c(r, np.float64)
+    idx = np.empty(k, dtype=np.int32)
+    w = np.empty(k, dtype=np.float64)
+    lib().orc_topk_softmax_f64(pr, r.size, k, idx.ctypes.data, w.ctypes.data)
+    return idx, w
+
+
 def argmax(v) -> int:
     v = np.ascontiguousarray(v)
     if v.dtype == np.float64:
@@ -138,7 +171,8 @@ def argmax(v) -> int:
 
 
 class Model:
-    """The oracle decoder over borrowed fp16 weights (dict from synth.model_weights)."""
+    """The oracle decoder over borrowed weights (dict from synth.model_weights, or synth.moe_weights for a
+    sparse-MoE config)."""
 
     def __init__(self, cfg, weights: dict, max_seq: int, precision: int = 32):
         self.cfg, self.precision, self.max_seq = cfg, precision, max_seq
@@ -146,8 +180,11 @@ class Model:
         L = cfg.n_layers
         self._arrays = {}
         ptrs = {}
+        moe = getattr(cfg, "n_experts", 0) > 0
         for name in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
-            arr = (P * max(L, 1))(*[weights["layers"][l][name].ctypes.data for l in range(L)])
+            # a MoE model has no dense FFN matrices: null pointers, never read
+            arr = (P * max(L, 1))(*[(None if moe and name in ("w_gate", "w_up", "w_down")
+                                     else weights["layers"][l][name].ctypes.data) for l in range(L)])
             self._arrays[name] = arr
             ptrs[name] = ctypes.cast(arr, P)
         self._w = OrcWeights(embed=weights["embed"].ctypes.data, lm_head=weights["lm_head"].ctypes.data,
@@ -157,6 +194,18 @@ class Model:
         self._h = lib().orc_create(ctypes.byref(self._c), ctypes.byref(self._w), precision)
         if not self._h:
             raise ValueError("oracle rejected the configuration")
+        if moe:
+            mp = {}
+            for name, key in (("router", "router"), ("gate_q", "gate_q"), ("up_q", "up_q"), ("down_q", "down_q"),
+                              ("gate_s", "gate_s"), ("up_s", "up_s"), ("down_s", "down_s")):
+                arrs = [np.ascontiguousarray(weights["layers"][l][key]) for l in range(L)]
+                self._arrays["moe_" + name] = arrs
+                tbl = (P * max(L, 1))(*[a.ctypes.data for a in arrs])
+                self._arrays["moe_" + name + "_tbl"] = tbl
+                mp[name] = ctypes.cast(tbl, P)
+            self._moe = OrcMoe(cfg.n_experts, cfg.top_k, cfg.expert_ffn, **mp)
+            if lib().orc_set_moe(self._h, ctypes.byref(self._moe)) != 0:
+                raise ValueError("oracle rejected the MoE description")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -182,6 +231,13 @@ class Model:
         for t in tokens:
             logits = self.forward(t)
         return logits
+
+    def moe_ffn(self, layer: int, u) -> np.ndarray:
+        """The sparse-MoE FFN output of `layer` for a normalised input u."""
+        u = np.ascontiguousarray(u, dtype=_real(self.precision))
+        out = np.empty(self.cfg.d_model, dtype=_real(self.precision))
+        lib().orc_moe_ffn(self._h, layer, u.ctypes.data, out.ctypes.data)
+        return out
 
     def kv_row(self, layer: int, kv: int, head: int, pos: int) -> np.ndarray:
         out = np.empty(self.cfg.head_dim, dtype=np.uint16)

@@ -16,6 +16,13 @@
  *
  * Precision: fp16 weights and K/V cache, arithmetic in REAL = float (orc_*_f32) or double (orc_*_f64).
  * Build with -ffp-contract=off so that every product and sum is rounded as written.
+ *
+ * Sparse-MoE layers (orc_set_moe; the pages' "Extending to frontier MoE models" section of the Kog blog post
+ * and the MoE projection of the creeta article's "2B demo vs frontier scale" section): the FFN of a layer is
+ *   r = W_router u (fp16 router); S = the top_k experts by r (lowest index first on ties);
+ *   w_e = softmax over {r_e : e in S}; x += sum_{e in S} w_e * Wd_e (silu(Wg_e u) * (Wu_e u)),
+ * where an expert weight is E4M3(q) * s_row (OCP FP8 E4M3, per-output-row fp32 scale), applied as
+ * y_row = s_row * sum_k E4M3(q_row,k) x_k.
  */
 #include <math.h>
 #include <stdint.h>
@@ -36,14 +43,26 @@ typedef struct {
   const uint16_t *const *ffn_norm, *const *w_gate, *const *w_up, *const *w_down;
 } orc_weights;
 
+/* Sparse-MoE FFN weights (borrowed), per layer: router [E][d] fp16; gate/up [E][F_e][d] and down [E][d][F_e]
+ * E4M3 codes; gate_s/up_s [E][F_e] and down_s [E][d] row scales. */
+typedef struct {
+  int n_experts, top_k, expert_ffn;
+  const uint16_t *const *router;
+  const uint8_t *const *gate_q, *const *up_q, *const *down_q;
+  const float *const *gate_s, *const *up_s, *const *down_s;
+} orc_moe;
+
 typedef struct {
   orc_config cfg;
   orc_weights w; /* borrowed: the caller keeps every tensor alive */
+  orc_moe moe;   /* n_experts == 0: dense FFN */
+  const void **moe_ptrs; /* owned copies of the MoE per-layer pointer arrays */
   const uint16_t **ptrs; /* owned copies of the per-layer pointer arrays */
   int precision;         /* 32 or 64 */
   int pos;
   uint16_t *kv; /* [L][2][Hkv][max_seq][dh] fp16 bits */
   void *x, *u, *q, *k, *v, *o, *t, *g, *up, *scores;
+  void *rl, *acc; /* MoE: router logits [E], FFN output [d] */
 } orc_model;
 
 /* ---- binary16 <-> real, from the format's definition ---------------------------------------------- */
@@ -70,6 +89,29 @@ static void half_init(void) {
 }
 
 static inline float half_value(uint16_t h) { return half_table[h]; }
+
+/* ---- OCP FP8 E4M3 ("fn": no infinities, 0x7F / 0xFF NaN) -> real, from the format's definition ---------- */
+
+static double e4m3_table[256];
+static int e4m3_table_ready = 0;
+
+static double e4m3_decode(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, f = b & 7;
+  double v;
+  if (e == 15 && f == 7)
+    v = NAN;
+  else if (e == 0)
+    v = ldexp((double)f, -9); /* subnormal: f/8 * 2^-6 */
+  else
+    v = ldexp(1.0 + f / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+static void e4m3_init(void) {
+  if (e4m3_table_ready) return;
+  for (int i = 0; i < 256; ++i) e4m3_table[i] = e4m3_decode((uint8_t)i);
+  e4m3_table_ready = 1;
+}
 
 /* Round a real to the nearest binary16 (ties to even) by scaling to the format's quantum at that
  * magnitude and rounding to an integer there (nearbyint in the default round-to-nearest-even mode). */
@@ -214,6 +256,9 @@ orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision
 void orc_destroy(orc_model *m) {
   if (!m) return;
   free(m->ptrs);
+  free(m->moe_ptrs);
+  free(m->rl);
+  free(m->acc);
   free(m->kv);
   free(m->x); free(m->u); free(m->q); free(m->k); free(m->v);
   free(m->o); free(m->t); free(m->g); free(m->up); free(m->scores);
@@ -241,3 +286,62 @@ void orc_kv_row(const orc_model *m, int layer, int kv, int head, int pos, uint16
   const uint16_t *p = m->kv + ((size_t)layer * 2 + kv) * c->n_kv_heads * S + head * S + (size_t)pos * c->head_dim;
   memcpy(out, p, sizeof(uint16_t) * (size_t)c->head_dim);
 }
+
+/* ---- sparse-MoE layers ------------------------------------------------------------------------------------- */
+
+/* Give the model sparse-MoE FFN layers (replacing the dense ones). Pointers are borrowed. Returns 0, or -1 for
+ * an invalid description (top_k outside 1..min(n_experts, 64), n_experts > 64, expert_ffn < 1). */
+int orc_set_moe(orc_model *m, const orc_moe *moe) {
+  e4m3_init();
+  if (!m || !moe || moe->n_experts < 1 || moe->n_experts > 64 || moe->top_k < 1 || moe->top_k > moe->n_experts ||
+      moe->expert_ffn < 1)
+    return -1;
+  const int L = m->cfg.n_layers > 0 ? m->cfg.n_layers : 1;
+  free(m->moe_ptrs);
+  m->moe_ptrs = (const void **)calloc((size_t)7 * L, sizeof(void *));
+  m->moe = *moe;
+  const void *const *src[7] = {(const void *const *)moe->router, (const void *const *)moe->gate_q,
+                               (const void *const *)moe->up_q, (const void *const *)moe->down_q,
+                               (const void *const *)moe->gate_s, (const void *const *)moe->up_s,
+                               (const void *const *)moe->down_s};
+  for (int j = 0; j < 7; ++j)
+    for (int l = 0; l < m->cfg.n_layers; ++l) m->moe_ptrs[(size_t)j * L + l] = src[j][l];
+  m->moe.router = (const uint16_t *const *)(m->moe_ptrs + 0 * (size_t)L);
+  m->moe.gate_q = (const uint8_t *const *)(m->moe_ptrs + 1 * (size_t)L);
+  m->moe.up_q = (const uint8_t *const *)(m->moe_ptrs + 2 * (size_t)L);
+  m->moe.down_q = (const uint8_t *const *)(m->moe_ptrs + 3 * (size_t)L);
+  m->moe.gate_s = (const float *const *)(m->moe_ptrs + 4 * (size_t)L);
+  m->moe.up_s = (const float *const *)(m->moe_ptrs + 5 * (size_t)L);
+  m->moe.down_s = (const float *const *)(m->moe_ptrs + 6 * (size_t)L);
+  const size_t es = m->precision == 32 ? sizeof(float) : sizeof(double);
+  const int d = m->cfg.d_model, Fe = moe->expert_ffn;
+  const int gmax = Fe > m->cfg.ffn_dim ? Fe : m->cfg.ffn_dim;
+  free(m->g);
+  free(m->up);
+  m->g = calloc((size_t)gmax, es);
+  m->up = calloc((size_t)gmax, es);
+  free(m->rl);
+  free(m->acc);
+  m->rl = calloc((size_t)moe->n_experts, es);
+  m->acc = calloc((size_t)d, es);
+  return 0;
+}
+
+/* The MoE FFN output of layer l for a given normalised input u (float or double by the model's precision). */
+void orc_moe_ffn(orc_model *m, int layer, const void *u, void *out) {
+  if (m->precision == 32)
+    moe_ffn_f32(m, layer, (const float *)u, (float *)out);
+  else
+    moe_ffn_f64(m, layer, (const double *)u, (double *)out);
+}
+
+double orc_e4m3_to_double(uint8_t b) { return e4m3_decode(b); }
+void orc_gemv_fp8_f64(const uint8_t *W, const float *s, const double *x, int M, int K, double *y) {
+  e4m3_init();
+  gemv_fp8_f64(W, s, x, M, K, y);
+}
+void orc_gemv_fp8_f32(const uint8_t *W, const float *s, const float *x, int M, int K, float *y) {
+  e4m3_init();
+  gemv_fp8_f32(W, s, x, M, K, y);
+}
+void orc_topk_softmax_f64(const double *r, int n, int top_k, int *idx, double *w) { topk_softmax_f64(r, n, top_k, idx, w); }

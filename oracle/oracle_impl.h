@@ -68,6 +68,59 @@ static void NAME(attention)(const REAL *q, const uint16_t *K, const uint16_t *V,
 /* silu(z) = z / (1 + exp(-z)). */
 static REAL NAME(silu)(REAL z) { return z / ((REAL)1 + EXP(-z)); }
 
+/* y = dequant(W) x for E4M3 codes W [M][K] with row scales s [M]: y_r = s_r * sum_k E4M3(W_rk) x_k, in order. */
+static void NAME(gemv_fp8)(const uint8_t *W, const float *s, const REAL *x, int M, int K, REAL *y) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < M; ++r) {
+    const uint8_t *row = W + (size_t)r * K;
+    REAL acc = 0;
+    for (int k = 0; k < K; ++k) acc += (REAL)e4m3_table[row[k]] * x[k];
+    y[r] = (REAL)s[r] * acc;
+  }
+}
+
+/* The top_k largest of r[0..n) (the lowest index first among equal values), in descending order, and the
+ * softmax over the selected values (max-subtracted). */
+static void NAME(topk_softmax)(const REAL *r, int n, int top_k, int *idx, REAL *w) {
+  for (int j = 0; j < top_k; ++j) {
+    int best = -1;
+    for (int e = 0; e < n; ++e) {
+      int taken = 0;
+      for (int i = 0; i < j; ++i) taken |= idx[i] == e;
+      if (!taken && (best < 0 || r[e] > r[best])) best = e;
+    }
+    idx[j] = best;
+  }
+  REAL mx = r[idx[0]], sum = 0;
+  for (int j = 1; j < top_k; ++j) mx = r[idx[j]] > mx ? r[idx[j]] : mx;
+  for (int j = 0; j < top_k; ++j) {
+    w[j] = EXP(r[idx[j]] - mx);
+    sum += w[j];
+  }
+  for (int j = 0; j < top_k; ++j) w[j] /= sum;
+}
+
+/* The sparse-MoE FFN of layer l on the normalised input u: out = sum_{e in top_k} w_e Wd_e (silu(Wg_e u) *
+ * (Wu_e u)), the experts taken in the order topk_softmax returns them. */
+static void NAME(moe_ffn)(orc_model *m, int l, const REAL *u, REAL *out) {
+  const orc_moe *mo = &m->moe;
+  const int d = m->cfg.d_model, Fe = mo->expert_ffn, E = mo->n_experts;
+  REAL *rl = (REAL *)m->rl, *g = (REAL *)m->g, *up = (REAL *)m->up, *t = (REAL *)m->t;
+  int idx[64];
+  REAL w[64];
+  NAME(gemv)(mo->router[l], u, E, d, rl);
+  NAME(topk_softmax)(rl, E, mo->top_k, idx, w);
+  for (int i = 0; i < d; ++i) out[i] = 0;
+  for (int j = 0; j < mo->top_k; ++j) {
+    const int e = idx[j];
+    NAME(gemv_fp8)(mo->gate_q[l] + (size_t)e * Fe * d, mo->gate_s[l] + (size_t)e * Fe, u, Fe, d, g);
+    NAME(gemv_fp8)(mo->up_q[l] + (size_t)e * Fe * d, mo->up_s[l] + (size_t)e * Fe, u, Fe, d, up);
+    for (int i = 0; i < Fe; ++i) g[i] = NAME(silu)(g[i]) * up[i];
+    NAME(gemv_fp8)(mo->down_q[l] + (size_t)e * d * Fe, mo->down_s[l] + (size_t)e * d, g, d, Fe, t);
+    for (int i = 0; i < d; ++i) out[i] += w[j] * t[i];
+  }
+}
+
 /* One decoder forward of `token` at position m->pos: appends K and V (rounded to fp16) to the cache,
  * writes the logits of the next position, advances pos. */
 static void NAME(forward)(orc_model *m, int token, REAL *logits) {
@@ -102,6 +155,12 @@ static void NAME(forward)(orc_model *m, int token, REAL *logits) {
     for (int i = 0; i < d; ++i) x[i] += t[i];
 
     NAME(rmsnorm)(x, m->w.ffn_norm[l], d, (REAL)c->rms_eps, u);
+    if (m->moe.n_experts > 0) {
+      REAL *acc = (REAL *)m->acc;
+      NAME(moe_ffn)(m, l, u, acc);
+      for (int i = 0; i < d; ++i) x[i] += acc[i];
+      continue;
+    }
     NAME(gemv)(m->w.w_gate[l], u, F, d, g);
     NAME(gemv)(m->w.w_up[l], u, F, d, up);
     for (int i = 0; i < F; ++i) g[i] = NAME(silu)(g[i]) * up[i];

@@ -13,7 +13,7 @@ import subprocess
 
 import numpy as np
 
-from .configs import GemvShape, ModelConfig, Workload  # noqa: F401  (re-export)
+from .configs import GemvShape, ModelConfig, MoEConfig, Workload  # noqa: F401  (re-export)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "synth.c")
@@ -25,8 +25,16 @@ TID_EMBED, TID_LM_HEAD, TID_FINAL_NORM, TID_PROMPT = 1, 2, 3, 0xFFFF
 LAYER_TENSORS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
 
 
+TID_ROUTER_SLOT = len(LAYER_TENSORS)  # the router of layer l has layer tensor slot 9
+EXPERT_KINDS = ("gate", "up", "down")
+
+
 def layer_tid(layer: int, name: str) -> int:
     return 16 + 16 * layer + LAYER_TENSORS.index(name)
+
+
+def expert_tid(layer: int, expert: int, kind: str) -> int:
+    return 0x10000000 + (layer * 4096 + expert) * 4 + EXPERT_KINDS.index(kind)
 
 
 def build_cmd() -> list[str]:
@@ -53,6 +61,9 @@ def lib():
         L.synth_splitmix64_next.restype = u64
         L.synth_f32_to_f16.argtypes = [ctypes.c_float]
         L.synth_f32_to_f16.restype = ctypes.c_uint16
+        L.synth_e4m3_rows.argtypes = [u64, u64, i64, i64, dbl, ctypes.c_void_p, ctypes.c_void_p]
+        L.synth_f32_to_e4m3.argtypes = [ctypes.c_float]
+        L.synth_f32_to_e4m3.restype = ctypes.c_uint8
         _lib = L
     return _lib
 
@@ -77,8 +88,9 @@ def tokens(seed: int, n: int, vocab: int, tensor_id: int = TID_PROMPT) -> np.nda
     return out
 
 
-def model_weights(cfg: ModelConfig) -> dict:
-    """All weights of a Llama-style decoder as fp16 bit patterns, row-major [out, in].
+def model_weights(cfg: ModelConfig, ffn: bool = True) -> dict:
+    """All weights of a Llama-style decoder as fp16 bit patterns, row-major [out, in] (without the dense FFN
+    matrices when ffn is False).
 
     Projections, embedding and LM head are N(0, weight_std). RMSNorm gains are exactly 1 when gain_std
     is 0, else 1 + N(0, gain_std).
@@ -103,16 +115,45 @@ def model_weights(cfg: ModelConfig) -> dict:
             "wv": w(t("wv"), (cfg.n_kv_heads * dh, d)),
             "wo": w(t("wo"), (d, cfg.n_heads * dh)),
             "ffn_norm": gain(t("ffn_norm")),
-            "w_gate": w(t("w_gate"), (cfg.ffn_dim, d)),
-            "w_up": w(t("w_up"), (cfg.ffn_dim, d)),
-            "w_down": w(t("w_down"), (d, cfg.ffn_dim)),
         })
+        if ffn:
+            layers[-1].update({
+                "w_gate": w(t("w_gate"), (cfg.ffn_dim, d)),
+                "w_up": w(t("w_up"), (cfg.ffn_dim, d)),
+                "w_down": w(t("w_down"), (d, cfg.ffn_dim)),
+            })
     return {
         "embed": w(TID_EMBED, (cfg.vocab, d)),
         "lm_head": w(TID_LM_HEAD, (cfg.vocab, d)),
         "final_norm": gain(TID_FINAL_NORM),
         "layers": layers,
     }
+
+
+def e4m3_rows(seed: int, tensor_id: int, rows: int, cols: int, std: float):
+    """FP8 weight rows: (q uint8 [rows, cols] E4M3 codes, scale float32 [rows]); weight = E4M3(q) * scale."""
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    lib().synth_e4m3_rows(seed, tensor_id, rows, cols, std, q.ctypes.data, sc.ctypes.data)
+    return q, sc
+
+
+def moe_weights(cfg: MoEConfig) -> dict:
+    """A sparse-MoE decoder's weights: attention, norms, embedding and LM head as in model_weights (fp16),
+    per layer a router [n_experts, d] (fp16, N(0, weight_std)) and the experts' FP8 matrices with row scales,
+    stacked over experts: gate_q/up_q [E, F_e, d], down_q [E, d, F_e] (uint8), gate_s/up_s [E, F_e],
+    down_s [E, d] (float32); every expert weight is N(0, weight_std) before quantisation."""
+    s, d, Fe, E = cfg.seed, cfg.d_model, cfg.expert_ffn, cfg.n_experts
+    base = model_weights(cfg, ffn=False)
+    for l, lay in enumerate(base["layers"]):
+        lay["router"] = normal_f16(s, 16 + 16 * l + TID_ROUTER_SLOT, (E, d), 0.0, cfg.weight_std)
+        for kind, (rows, cols) in (("gate", (Fe, d)), ("up", (Fe, d)), ("down", (d, Fe))):
+            q = np.empty((E, rows, cols), dtype=np.uint8)
+            sc = np.empty((E, rows), dtype=np.float32)
+            for e in range(E):
+                q[e], sc[e] = e4m3_rows(s, expert_tid(l, e, kind), rows, cols, cfg.weight_std)
+            lay[kind + "_q"], lay[kind + "_s"] = q, sc
+    return base
 
 
 def prompt(wl: Workload) -> np.ndarray:

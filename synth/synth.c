@@ -12,9 +12,12 @@
  *     with r = sqrt(-2 ln u1), t = 2*pi*u2, u1 = U(draw 2j), u2 = U(draw 2j+1), U(z) = ((z >> 11) + 0.5) / 2^53.
  *   - value = mean + std * z in fp64, rounded to fp32, then to fp16 with round-to-nearest-even.
  *   - Token ids: draw i mod vocab.
+ *   - FP8 expert weights (the sparse-MoE model): fp32 values as above, quantised per row to E4M3 with a
+ *     fp32 scale (synth_e4m3_rows); the model's weight is the E4M3 value times the row's scale.
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define GOLDEN 0x9E3779B97F4A7C15ULL
@@ -82,6 +85,52 @@ void synth_tokens(uint64_t seed, uint64_t tensor_id, int64_t n, int64_t modulo, 
   uint64_t base = stream_base(seed, tensor_id);
   for (int64_t i = 0; i < n; ++i) out[i] = (int32_t)(draw(base, (uint64_t)i) % (uint64_t)modulo);
 }
+
+/* fp32 -> OCP FP8 E4M3 ("fn" variant: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * largest finite 448, NaN 0x7F), round to nearest with ties to even, saturating at +-448. */
+static uint8_t to_e4m3(float f) {
+  if (isnan(f)) return 0x7F;
+  const uint8_t sign = signbit(f) ? 0x80 : 0;
+  const double a = fabs((double)f);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < 0.015625) return sign | (uint8_t)rint(a * 512.0); /* below 2^-6: steps of 2^-9; 8 is code 0x08 */
+  int e;
+  const double m = frexp(a, &e); /* a = m 2^e, 0.5 <= m < 1 */
+  int E = e - 1;                  /* a = (1 + frac) 2^E, E in [-6, 8] */
+  double q = rint((2.0 * m - 1.0) * 8.0);
+  if (q == 8.0) {
+    q = 0.0;
+    E += 1;
+  }
+  if (E > 8 || (E == 8 && q > 6.0)) return sign | 0x7E;
+  return sign | (uint8_t)(((E + 7) << 3) | (int)q);
+}
+
+/* Rows of an FP8 weight matrix with a per-row fp32 scale: w = fp32(std * N_i) for element i = r * cols + c,
+ * scale[r] = max_c |w| / 448 (1 if the row is zero), q[r][c] = E4M3(w / scale[r]). The stored model weight is
+ * then E4M3(q) * scale[r]. */
+void synth_e4m3_rows(uint64_t seed, uint64_t tensor_id, int64_t rows, int64_t cols, double std, uint8_t *q,
+                     float *scale) {
+  uint64_t base = stream_base(seed, tensor_id);
+#pragma omp parallel
+  {
+    float *w = (float *)malloc((size_t)cols * sizeof(float));
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+      float amax = 0.f;
+      for (int64_t c = 0; c < cols; ++c) {
+        w[c] = (float)(std * normal_at(base, (uint64_t)(r * cols + c)));
+        amax = fmaxf(amax, fabsf(w[c]));
+      }
+      const float sc = amax > 0.f ? amax / 448.0f : 1.0f;
+      scale[r] = sc;
+      for (int64_t c = 0; c < cols; ++c) q[r * cols + c] = to_e4m3(w[c] / sc);
+    }
+    free(w);
+  }
+}
+
+uint8_t synth_f32_to_e4m3(float f) { return to_e4m3(f); }
 
 /* Raw access for the generator's own tests. */
 uint64_t synth_draw(uint64_t seed, uint64_t tensor_id, uint64_t i) { return draw(stream_base(seed, tensor_id), i); }
