@@ -10,6 +10,8 @@ L2 and every token streams them all, so no L2 flush is needed between steps.
 workload. With N > 1 (torchrun) every rank runs an independent replica: the path has no data exchange.
 
 Other modes (not the headline line): --long runs the long-context workload (prompt 8,192, 512 new tokens);
+--moe the sparse-MoE workload (24 layers, 64 FP8 experts of width 1,024, top 4; prompt 256, 512 new tokens),
+whose MBU counts the bytes a token actually streams (attention, router, the 4 routed experts, LM head);
 --gemv-sweep prints one JSON line per standalone GEMV shape (GB/s, cold HBM); --phase-gemv does the same for
 the decode's five projection shapes of the 2B model (the phase-split view of the weight stream).
 """
@@ -29,6 +31,7 @@ sys.path.insert(0, ROOT)
 METRIC = "batch-1 decode tok/s, 2B fp16 on 1 GB300; MBU vs HBM peak"
 WORKLOAD = "llama2b_p128_n1024"
 PROMPT, NEW = 128, 1024
+MOE_METRIC = "batch-1 decode tok/s, sparse MoE (64 FP8 experts, top 4) on 1 GB300; MBU over active bytes"
 
 
 def measured_peaks():
@@ -42,8 +45,19 @@ def measured_peaks():
 def phase_bytes(model, c):
     """Algorithmic bytes of each phase of one layer (and of the LM head) at c attended positions."""
     d, dh, F = model.d_model, model.head_dim, model.ffn_dim
-    return {"qkv": 2 * (model.n_heads + 2 * model.n_kv_heads) * dh * d, "att": 2 * 2 * model.n_kv_heads * dh * c,
-            "wo": 2 * d * model.n_heads * dh, "gu": 2 * 2 * F * d, "down": 2 * d * F, "lm": 2 * model.vocab * d}
+    out = {"qkv": 2 * (model.n_heads + 2 * model.n_kv_heads) * dh * d, "att": 2 * 2 * model.n_kv_heads * dh * c,
+           "wo": 2 * d * model.n_heads * dh, "gu": 2 * 2 * F * d, "down": 2 * d * F, "lm": 2 * model.vocab * d}
+    if getattr(model, "n_experts", 0):
+        k = model.top_k
+        out.update(router=2 * model.n_experts * d, egu=k * (2 * F * d + 4 * 2 * F), edown=k * (d * F + 4 * d))
+    return out
+
+
+def phase_names(model):
+    """The grid phases of one layer, in order."""
+    if getattr(model, "n_experts", 0):
+        return ["qkv", "att", "wo", "router", "egu", "edown"]
+    return ["qkv", "att", "wo", "gu", "down"]
 
 
 def phase_breakdown(dec, model, prompt_len, new):
@@ -51,19 +65,19 @@ def phase_breakdown(dec, model, prompt_len, new):
     runs from the earliest departure from the previous barrier to the last arrival at its own; the release
     latency is the gap between the last arrival at a barrier and the earliest departure from it."""
     import numpy as np
-    per_tok = 5 * model.n_layers + 1
+    names = phase_names(model)
+    per_tok = len(names) * model.n_layers + 1
     toks = min(new, 4096 // per_tok)
     if toks < 2:
         return None
     arrive, wait = dec.barrier_trace(0, toks * per_tok)
     arrive = arrive.astype(np.float64)
     leave = arrive + wait
-    names = ["qkv", "att", "wo", "gu", "down"]
     per = {n: [] for n in names + ["lm"]}
     release = []
     for k in range(1, arrive.shape[0]):
         j = k % per_tok
-        name = "lm" if j == per_tok - 1 else names[j % 5]
+        name = "lm" if j == per_tok - 1 else names[j % len(names)]
         per[name].append((arrive[k].max() - leave[k - 1].min()) / 1e3)
         release.append((leave[k].min() - arrive[k].max()) / 1e3)
     c_mid = prompt_len + 1 + toks // 2
@@ -274,16 +288,17 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_sample(seconds_budget=15.0, max_forwards=400):
-    """The oracle as it stands on the host cores: greedy decode forwards of the 2B model, for about
-    seconds_budget of CPU time (at most max_forwards)."""
+def cpu_baseline_sample(seconds_budget=15.0, max_forwards=400, model=None, weights=None):
+    """The oracle as it stands on the host cores: greedy decode forwards of the 2B model (or `model` with
+    `weights`), for about seconds_budget of CPU time (at most max_forwards)."""
     import oracle
     import synth
     from synth.configs import TWO_B
 
-    w = synth.model_weights(TWO_B)
-    prompt = synth.tokens(TWO_B.seed, 8, TWO_B.vocab)
-    m = oracle.Model(TWO_B, w, len(prompt) + max_forwards + 1, 32)
+    if model is None:
+        model, weights = TWO_B, synth.model_weights(TWO_B)
+    prompt = synth.tokens(model.seed, 8, model.vocab)
+    m = oracle.Model(model, weights, len(prompt) + max_forwards + 1, 32)
     cur = m.prefill(prompt)
     n, t0 = 0, time.perf_counter()
     while n < max_forwards:
@@ -293,7 +308,7 @@ def cpu_baseline_sample(seconds_budget=15.0, max_forwards=400):
             break
     dt = time.perf_counter() - t0
     return {"value": n / dt, "unit": "tok/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{n} greedy decode forwards of the 2B model after an 8-token prefill ({dt:.1f} s)"}
+            "sample": f"{n} greedy decode forwards of the {model.name} model after an 8-token prefill ({dt:.1f} s)"}
 
 
 def main():
@@ -307,12 +322,17 @@ def main():
     ap.add_argument("--prompt", type=int, default=PROMPT)
     ap.add_argument("--decode", type=int, default=NEW)
     ap.add_argument("--long", action="store_true", help="the long-context workload: prompt 8,192, 512 new tokens")
+    ap.add_argument("--moe", action="store_true",
+                    help="the sparse-MoE workload (64 FP8 experts, top 4): prompt 256, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
     ap.add_argument("--phase-gemv", action="store_true",
                     help="the decode's five projection shapes of the 2B model through the standalone GEMV (GB/s each)")
     args = ap.parse_args()
     if args.long:
         args.prompt, args.decode = 8192, 512
+    if args.moe:
+        args.prompt = 256 if args.prompt == PROMPT else args.prompt
+        args.decode = 512 if args.decode == NEW else args.decode
     if args.gemv_sweep:
         gemv_sweep(args)
         return
@@ -331,13 +351,19 @@ def main():
 
     import persistent_monokernel_decode_gb300 as kie
     import synth
-    from synth.configs import TWO_B
+    from synth.configs import MOE_M, TWO_B
 
-    model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
     prompt_len, new = args.prompt, args.decode
-    workload = WORKLOAD if (args.layers, prompt_len, new) == (25, PROMPT, NEW) else \
-        ("llama2b_p8192_n512" if (args.layers, prompt_len, new) == (25, 8192, 512) else
-         f"llama2b_L{args.layers}_p{prompt_len}_n{new}")
+    if args.moe:
+        layers = MOE_M.n_layers if args.layers == 25 else args.layers
+        model = MOE_M if layers == MOE_M.n_layers else dataclasses.replace(MOE_M, n_layers=layers)
+        workload = "moe_p256_n512" if (layers, prompt_len, new) == (24, 256, 512) else \
+            f"moe_L{layers}_p{prompt_len}_n{new}"
+    else:
+        model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
+        workload = WORKLOAD if (args.layers, prompt_len, new) == (25, PROMPT, NEW) else \
+            ("llama2b_p8192_n512" if (args.layers, prompt_len, new) == (25, 8192, 512) else
+             f"llama2b_L{args.layers}_p{prompt_len}_n{new}")
 
     torch.cuda.set_device(local)
     pg = None
@@ -347,10 +373,11 @@ def main():
         pg = dist
     kie.build()
 
-    w = synth.model_weights(model)
+    w = synth.moe_weights(model) if args.moe else synth.model_weights(model)
     prompt = synth.tokens(model.seed, prompt_len, model.vocab)
     dec = kie.Decoder(model, w, max_seq=prompt_len + new)
-    del w
+    if not args.moe:
+        del w
     out = torch.empty(new, dtype=torch.int32, device="cuda")
     stream = dec.stream
 
@@ -405,11 +432,14 @@ def main():
     bytes_launch = algorithmic_bytes(model, prompt_len, new)
     achieved = bytes_launch / step_s / 1e9
     line = {
-        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "metric": MOE_METRIC if args.moe else METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload, "prompt": prompt_len, "decode_tokens": new, "weights": "fp16",
-                   "kv_cache": "fp16", "l2": "no flush: 3.9 GB of weights (> 129 MB L2) streamed per token",
+        "config": {"workload": workload, "prompt": prompt_len, "decode_tokens": new,
+                   "weights": "fp16 attention/router/LM head, FP8 E4M3 experts" if args.moe else "fp16",
+                   "kv_cache": "fp16",
+                   "l2": (f"no flush: {model.weight_bytes_per_token() / 1e9:.2f} GB of weights (> 129 MB L2) "
+                          "streamed per token"),
                    "parallelism": "replicas" if world > 1 else "single GPU", "n_cta": dec.n_cta},
         "e2e": {"value": replica_throughput(world, new, e2e_step), "unit": "tok/s", "h2d_bytes_per_step": prompt_len * 4,
                 "d2h_bytes_per_step": new * 4 + 8,
@@ -428,7 +458,7 @@ def main():
     }
     dec.close()
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample()
+        line["cpu_baseline"] = cpu_baseline_sample(model=model, weights=w) if args.moe else cpu_baseline_sample()
     emit(line, rank)
     if pg:
         pg.destroy_process_group()

@@ -184,6 +184,53 @@ int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, in
 #define KIE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
 int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
 
+/* ---- sparse-MoE models with FP8 experts ----------------------------------------------------------------
+ * The "Extending to frontier MoE models" section of the Kog blog post ("the 2B demo vs frontier scale" in the
+ * Creeta write-up) projects the monokernel onto sparse mixture-of-experts models with FP8 weights; the pages
+ * give no kernel for it. This library reads it as: the FFN of every layer is n_experts SwiGLU experts of width
+ * cfg->ffn_dim; a router (fp16 [n_experts, d_model]) scores the FFN-normalised vector u, the top_k experts are
+ * taken (largest logit first, the lowest id among equal logits) and weighted by the softmax of their logits;
+ * expert weights are OCP FP8 E4M3 ("fn": no infinities, max 448) codes, one fp32 scale per row, the weight
+ * being code value * row scale. out = sum over the routed experts j of w_j * Wd_j (silu(Wg_j u) * (Wu_j u)).
+ * Attention, norms, embedding and LM head are those of the dense model. Decode runs the same monokernel with
+ * the router, the top_k selection and the two expert projections as grid phases: after the router the
+ * producer warp streams only the routed experts' FP8 tiles.
+ *
+ * Requirements: 1 <= n_experts <= 256, 1 <= top_k <= min(8, n_experts), d_model and ffn_dim multiples of 16.
+ * Prefill of a MoE ctx runs the prompt through the decode kernel one position after another (teacher forcing,
+ * LM head at the last position only), in one launch per call. kie_decode_noalloc serves MoE ctxs too. */
+typedef struct {
+  int n_experts, top_k;
+} kie_moe_config;
+
+/* Host MoE weights: arrays of n_layers host pointers. router[l] fp16 bits [n_experts, d_model];
+ * gate_q[l], up_q[l] E4M3 codes [n_experts, ffn_dim, d_model]; down_q[l] codes [n_experts, d_model, ffn_dim];
+ * gate_s[l], up_s[l] fp32 row scales [n_experts, ffn_dim]; down_s[l] [n_experts, d_model]. The kie_weights
+ * passed alongside supply everything else; its w_gate, w_up and w_down are not read (may be NULL).
+ * Ownership: read during creation only. */
+typedef struct {
+  const uint16_t *const *router;
+  const uint8_t *const *gate_q, *const *up_q, *const *down_q;
+  const float *const *gate_s, *const *up_s, *const *down_s;
+} kie_moe_weights;
+
+/* kie_query_buffers for a sparse-MoE model (errors: INVALID for an unsupported cfg or moe, CUDA). */
+int kie_query_buffers_moe(const kie_config *cfg, const kie_moe_config *moe, int n_cta, kie_buffer_sizes *out);
+
+/* kie_create / kie_create_with_buffers for a sparse-MoE model: the expert matrices are packed per CTA in
+ * 512-code column blocks (kie_packed_offset_fp8), gate and up rows interleaved; the router and the FFN gains
+ * are stored as given (the gain multiplies the staged vector, not the FP8 weights). */
+int kie_create_moe(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w, const kie_moe_weights *mw,
+                   void *stream, kie_ctx **out);
+int kie_create_moe_with_buffers(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w,
+                                const kie_moe_weights *mw, void *stream, void *weights_dev, size_t weights_bytes,
+                                void *kv_dev, size_t kv_bytes, void *workspace_dev, size_t workspace_bytes,
+                                kie_ctx **out);
+
+/* Host-side layout query (no GPU needed): byte offset of code Q[r][c] inside a packed FP8 matrix [M, K]
+ * (column blocks of 512 codes). M even, K a multiple of 16; -1 for bad arguments. */
+int64_t kie_packed_offset_fp8(int M, int K, int n_cta, int r, int c);
+
 /* Host-side layout query (no GPU needed): element offset of W[r][c] inside the packed matrix. */
 int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c);
 

@@ -67,7 +67,7 @@ def lib():
             "orc_set_moe": ([P, ctypes.POINTER(OrcMoe)], i), "orc_moe_ffn": ([P, i, P, P], None),
             "orc_e4m3_to_double": ([ctypes.c_uint8], d),
             "orc_gemv_fp8_f32": ([P, P, P, i, i, P], None), "orc_gemv_fp8_f64": ([P, P, P, i, i, P], None),
-            "orc_topk_softmax_f64": ([P, i, i, P, P], None),
+            "orc_topk_softmax_f64": ([P, i, i, P, P], None), "orc_route_margin": ([P, i], d),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -238,6 +238,11 @@ class Model:
         out = np.empty(self.cfg.d_model, dtype=_real(self.precision))
         lib().orc_moe_ffn(self._h, layer, u.ctypes.data, out.ctypes.data)
         return out
+
+    def route_margin(self, reset: bool = True) -> float:
+        """Smallest routing margin (top_k-th router logit minus the best unselected one) over the MoE layers
+        evaluated since the last reset; +inf for a dense model or when every expert is selected."""
+        return lib().orc_route_margin(self._h, int(reset))
 
     def kv_row(self, layer: int, kv: int, head: int, pos: int) -> np.ndarray:
         out = np.empty(self.cfg.head_dim, dtype=np.uint16)

@@ -63,6 +63,7 @@ typedef struct {
   uint16_t *kv; /* [L][2][Hkv][max_seq][dh] fp16 bits */
   void *x, *u, *q, *k, *v, *o, *t, *g, *up, *scores;
   void *rl, *acc; /* MoE: router logits [E], FFN output [d] */
+  double route_margin; /* MoE diagnostic: smallest gap between the last selected and the best unselected logit */
 } orc_model;
 
 /* ---- binary16 <-> real, from the format's definition ---------------------------------------------- */
@@ -221,6 +222,7 @@ orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision
       cfg->vocab <= 0 || cfg->max_seq <= 0)
     return NULL;
   orc_model *m = (orc_model *)calloc(1, sizeof(orc_model));
+  if (m) m->route_margin = INFINITY;
   m->cfg = *cfg;
   m->precision = precision;
   int L = cfg->n_layers;
@@ -293,7 +295,7 @@ void orc_kv_row(const orc_model *m, int layer, int kv, int head, int pos, uint16
  * an invalid description (top_k outside 1..min(n_experts, 64), n_experts > 64, expert_ffn < 1). */
 int orc_set_moe(orc_model *m, const orc_moe *moe) {
   e4m3_init();
-  if (!m || !moe || moe->n_experts < 1 || moe->n_experts > 64 || moe->top_k < 1 || moe->top_k > moe->n_experts ||
+  if (!m || !moe || moe->n_experts < 1 || moe->n_experts > 1024 || moe->top_k < 1 || moe->top_k > moe->n_experts ||
       moe->expert_ffn < 1)
     return -1;
   const int L = m->cfg.n_layers > 0 ? m->cfg.n_layers : 1;
@@ -328,6 +330,15 @@ int orc_set_moe(orc_model *m, const orc_moe *moe) {
 }
 
 /* The MoE FFN output of layer l for a given normalised input u (float or double by the model's precision). */
+/* The smallest routing margin seen since the last call with reset != 0 (or since creation): over every MoE layer
+ * evaluated, the top_k-th largest router logit minus the largest unselected one (+inf when every expert is
+ * selected). A test uses it to tell routing decisions that rounding cannot change from near-ties. */
+double orc_route_margin(orc_model *m, int reset) {
+  const double v = m->route_margin;
+  if (reset) m->route_margin = INFINITY;
+  return v;
+}
+
 void orc_moe_ffn(orc_model *m, int layer, const void *u, void *out) {
   if (m->precision == 32)
     moe_ffn_f32(m, layer, (const float *)u, (float *)out);

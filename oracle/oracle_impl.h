@@ -106,10 +106,20 @@ static void NAME(moe_ffn)(orc_model *m, int l, const REAL *u, REAL *out) {
   const orc_moe *mo = &m->moe;
   const int d = m->cfg.d_model, Fe = mo->expert_ffn, E = mo->n_experts;
   REAL *rl = (REAL *)m->rl, *g = (REAL *)m->g, *up = (REAL *)m->up, *t = (REAL *)m->t;
-  int idx[64];
-  REAL w[64];
+  int idx[1024];
+  REAL w[1024];
   NAME(gemv)(mo->router[l], u, E, d, rl);
   NAME(topk_softmax)(rl, E, mo->top_k, idx, w);
+  {
+    double best_out = -INFINITY;
+    for (int e = 0; e < E; ++e) {
+      int taken = 0;
+      for (int j = 0; j < mo->top_k; ++j) taken |= idx[j] == e;
+      if (!taken && (double)rl[e] > best_out) best_out = (double)rl[e];
+    }
+    const double gap = (double)rl[idx[mo->top_k - 1]] - best_out;
+    if (gap < m->route_margin) m->route_margin = gap;
+  }
   for (int i = 0; i < d; ++i) out[i] = 0;
   for (int j = 0; j < mo->top_k; ++j) {
     const int e = idx[j];

@@ -104,6 +104,14 @@ class KieWeights(ctypes.Structure):
                                  "ffn_norm", "w_gate", "w_up", "w_down")]
 
 
+class KieMoeConfig(ctypes.Structure):
+    _fields_ = [("n_experts", ctypes.c_int), ("top_k", ctypes.c_int)]
+
+
+class KieMoeWeights(ctypes.Structure):
+    _fields_ = [(n, P) for n in ("router", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s")]
+
+
 class KieBufferSizes(ctypes.Structure):
     _fields_ = [("weights_bytes", ctypes.c_size_t), ("kv_bytes", ctypes.c_size_t),
                 ("workspace_bytes", ctypes.c_size_t), ("n_cta", ctypes.c_int)]
@@ -140,6 +148,11 @@ SIGNATURES = {
     "kie_decode_noalloc": ([P, ctypes.c_int, P], ctypes.c_int),
     "kie_packed_offset": ([ctypes.c_int] * 5, ctypes.c_int64),
     "kie_rows_of_cta": ([ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
+    "kie_query_buffers_moe": ([P, P, ctypes.c_int, P], ctypes.c_int),
+    "kie_create_moe": ([P, P, P, P, P, P], ctypes.c_int),
+    "kie_create_moe_with_buffers": ([P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P, ctypes.c_size_t, P],
+                                    ctypes.c_int),
+    "kie_packed_offset_fp8": ([ctypes.c_int] * 5, ctypes.c_int64),
 }
 
 _lib = None
@@ -178,20 +191,54 @@ def make_config(model, max_seq: int) -> KieConfig:
                      model.ffn_dim, model.vocab, max_seq, model.rope_theta, model.rms_eps)
 
 
-def kie_query_buffers(cfg: KieConfig, n_cta: int = 0) -> KieBufferSizes:
+def make_moe_config(model) -> KieMoeConfig:
+    return KieMoeConfig(model.n_experts, model.top_k)
+
+
+def is_moe(model) -> bool:
+    return getattr(model, "n_experts", 0) > 0
+
+
+def kie_query_buffers(cfg: KieConfig, n_cta: int = 0, moe: KieMoeConfig = None) -> KieBufferSizes:
     out = KieBufferSizes()
-    _check(lib().kie_query_buffers(ctypes.byref(cfg), n_cta, ctypes.byref(out)))
+    if moe is None:
+        _check(lib().kie_query_buffers(ctypes.byref(cfg), n_cta, ctypes.byref(out)))
+    else:
+        _check(lib().kie_query_buffers_moe(ctypes.byref(cfg), ctypes.byref(moe), n_cta, ctypes.byref(out)))
     return out
 
 
-class _HostWeights:
-    """ctypes view of a weights dict (fp16 bit arrays) that keeps every array alive."""
+def _pointer_table(keep: dict, name: str, arrays: list):
+    keep[name] = arrays
+    tbl = (P * max(len(arrays), 1))(*[a.ctypes.data for a in arrays])
+    keep[name + "_tbl"] = tbl
+    return ctypes.cast(tbl, P)
+
+
+class _HostMoeWeights:
+    """ctypes view of the sparse-MoE part of a weights dict (router fp16 bits, FP8 codes, fp32 row scales)."""
 
     def __init__(self, weights: dict, n_layers: int):
         self.keep = weights
         self.arrays = {}
+        dtypes = {"router": np.uint16, "gate_q": np.uint8, "up_q": np.uint8, "down_q": np.uint8,
+                  "gate_s": np.float32, "up_s": np.float32, "down_s": np.float32}
+        ptrs = {name: _pointer_table(self.arrays, name,
+                                     [np.ascontiguousarray(weights["layers"][l][name], dtype=dt) for l in range(n_layers)])
+                for name, dt in dtypes.items()}
+        self.struct = KieMoeWeights(**ptrs)
+
+
+class _HostWeights:
+    """ctypes view of a weights dict (fp16 bit arrays) that keeps every array alive. The dense FFN matrices are
+    left NULL when ffn is False (sparse-MoE models)."""
+
+    def __init__(self, weights: dict, n_layers: int, ffn: bool = True):
+        self.keep = weights
+        self.arrays = {}
         ptrs = {}
-        for name in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
+        names = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm") + (("w_gate", "w_up", "w_down") if ffn else ())
+        for name in names:
             arrs = [np.ascontiguousarray(weights["layers"][l][name], dtype=np.uint16) for l in range(n_layers)]
             self.arrays[name] = arrs
             tbl = (P * max(n_layers, 1))(*[a.ctypes.data for a in arrs])
@@ -214,21 +261,28 @@ class Decoder:
     """One decode context (kie_ctx): repacked weights, KV cache and workspace in torch-allocated HBM."""
 
     def __init__(self, model, weights: dict, max_seq: int, stream=None):
+        """model: a ModelConfig-like object; a sparse-MoE model (n_experts > 0, with top_k, and ffn_dim the expert
+        width) takes the weights of synth.moe_weights (router, FP8 experts with row scales)."""
         torch = _torch()
         self.model, self.max_seq = model, max_seq
         self.cfg = make_config(model, max_seq)
-        sizes = kie_query_buffers(self.cfg, 0)
+        self.moe = make_moe_config(model) if is_moe(model) else None
+        sizes = kie_query_buffers(self.cfg, 0, self.moe)
         dev = torch.device("cuda", torch.cuda.current_device())
         self._wbuf = torch.empty(sizes.weights_bytes, dtype=torch.uint8, device=dev)
         self._kvbuf = torch.empty(sizes.kv_bytes, dtype=torch.uint8, device=dev)
         self._wsbuf = torch.empty(sizes.workspace_bytes, dtype=torch.uint8, device=dev)
         self.stream = stream if stream is not None else torch.cuda.current_stream()
-        hw = _HostWeights(weights, model.n_layers)
+        hw = _HostWeights(weights, model.n_layers, ffn=self.moe is None)
         ctx = P()
-        rc = lib().kie_create_with_buffers(ctypes.byref(self.cfg), ctypes.byref(hw.struct),
-                                           P(self.stream.cuda_stream), self._wbuf.data_ptr(), sizes.weights_bytes,
-                                           self._kvbuf.data_ptr(), sizes.kv_bytes, self._wsbuf.data_ptr(),
-                                           sizes.workspace_bytes, ctypes.byref(ctx))
+        bufs = (P(self.stream.cuda_stream), self._wbuf.data_ptr(), sizes.weights_bytes, self._kvbuf.data_ptr(),
+                sizes.kv_bytes, self._wsbuf.data_ptr(), sizes.workspace_bytes, ctypes.byref(ctx))
+        if self.moe is None:
+            rc = lib().kie_create_with_buffers(ctypes.byref(self.cfg), ctypes.byref(hw.struct), *bufs)
+        else:
+            mw = _HostMoeWeights(weights, model.n_layers)
+            rc = lib().kie_create_moe_with_buffers(ctypes.byref(self.cfg), ctypes.byref(self.moe),
+                                                   ctypes.byref(hw.struct), ctypes.byref(mw.struct), *bufs)
         _check(rc, None)
         self.ctx = ctx
         self.n_cta = lib().kie_n_cta(ctx)
@@ -330,6 +384,10 @@ def gemv(packed, x, M: int, K: int, n_cta: int = 0, y=None):
 
 def packed_offset(M: int, K: int, n_cta: int, r: int, c: int) -> int:
     return lib().kie_packed_offset(M, K, n_cta, r, c)
+
+
+def packed_offset_fp8(M: int, K: int, n_cta: int, r: int, c: int) -> int:
+    return lib().kie_packed_offset_fp8(M, K, n_cta, r, c)
 
 
 def rows_of_cta(M: int, n_cta: int, cta: int):

@@ -21,6 +21,8 @@ cudaError_t kie_launch_gemv(const uint8_t *packed, const __half *x, float *y, in
                             unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t kie_launch_pack(const uint16_t *src, uint16_t *dst, int M, int K, int n_cta, const uint16_t *gain,
                             cudaStream_t stream);
+cudaError_t kie_launch_pack_fp8(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n_cta,
+                                cudaStream_t stream);
 
 namespace {
 
@@ -32,19 +34,22 @@ thread_local std::string g_create_error;
 
 size_t al(size_t v) { return kie::align_up(v, ALIGN); }
 
+// Byte offsets of the device weight buffer. Per layer (layer_stride apart): qkv, wo, then the dense FFN (gu,
+// down) or the sparse-MoE FFN (router, egu/edn: n_experts packed FP8 matrices egu_bytes/edn_bytes apart,
+// esgu/esdn: their row scales). Then the LM head, the embedding and (MoE) the fp32 FFN gains [L][d].
 struct WeightLayout {
-  size_t qkv, wo, gu, down, layer_stride, lm, embed, total;
+  size_t qkv, wo, gu, down, router, egu, edn, esgu, esdn, egu_bytes, edn_bytes, layer_stride, lm, embed, gffn, total;
 };
 
 struct WsLayout {
-  size_t x, h, q, o, a, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
+  size_t x, h, q, o, a, rlog, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
       pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, total;
   int pf_part_rows;
   int smax;
 };
 
 struct Plan {
-  int n_cta, nslot, vec_floats, out_floats, out_res, out_rope;
+  int n_cta, nslot, vec_floats, out_floats, out_res, out_rope, out_moe;
   size_t smem;
   WeightLayout w;
   WsLayout ws;
@@ -52,6 +57,14 @@ struct Plan {
 };
 
 int max_rows_per_cta(int M, int n) { return 2 * ((M / 2 + n - 1) / n); }
+
+const char *check_moe(const kie_config *c, const kie_moe_config *m) {
+  if (!m) return nullptr;
+  if (m->n_experts < 1 || m->n_experts > kie::MAX_EXPERTS) return "n_experts must be in [1, 256]";
+  if (m->top_k < 1 || m->top_k > kie::MAX_TOP_K || m->top_k > m->n_experts) return "top_k must be in [1, min(8, n_experts)]";
+  if (c->d_model % 16 || c->ffn_dim % 16) return "a sparse-MoE model needs d_model and ffn_dim multiples of 16";
+  return nullptr;
+}
 
 const char *check_config(const kie_config *c) {
   if (!c) return "config is NULL";
@@ -68,9 +81,11 @@ const char *check_config(const kie_config *c) {
   return nullptr;
 }
 
-const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) {
+// moe: null for a dense model.
+const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta, int smem_optin, Plan *pl) {
   const int d = c->d_model, dh = c->head_dim, dq = c->n_heads * dh, G = c->n_heads / c->n_kv_heads;
   const size_t L = (size_t)c->n_layers;
+  const int E = moe ? moe->n_experts : 0, topk = moe ? moe->top_k : 0, F = c->ffn_dim;
   pl->n_cta = n_cta;
   if (n_cta < c->n_kv_heads) return "the grid needs at least one CTA per KV head";
   // shared memory: ring + input vector (largest of d, F, Hq*dh, attention scratch) + row results
@@ -78,14 +93,16 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   // 3 x MAX_GROUP running values, and the merge's [smax][G] m/weight and l arrays
   const int smax = std::max(1, n_cta / c->n_kv_heads);
   const int att = G * dh + kie::ATT_SUB * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
-  pl->vec_floats = std::max(std::max(d, c->ffn_dim), std::max(dq, att));
-  // row results of the widest projection, then this CTA's slices of x and h, then the token's RoPE row
-  const int rows = std::max(std::max(max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta),
-                                     max_rows_per_cta(d, n_cta)),
-                            std::max(max_rows_per_cta(2 * c->ffn_dim, n_cta), max_rows_per_cta(c->vocab, n_cta)));
+  pl->vec_floats = std::max(std::max(std::max(d, c->ffn_dim), std::max(dq, att)), topk * F);
+  // row results of the widest projection (for MoE also top_k experts' rows side by side), then this CTA's slices
+  // of x and h, then the token's RoPE row, then (MoE) the expert selection and the routed experts' row scales
+  const int rows_gu = max_rows_per_cta(2 * F, n_cta), rows_d = max_rows_per_cta(d, n_cta);
+  const int rows = std::max({max_rows_per_cta((c->n_heads + 2 * c->n_kv_heads) * dh, n_cta), rows_d, rows_gu,
+                             max_rows_per_cta(c->vocab, n_cta), topk * rows_gu, topk * rows_d});
   pl->out_res = (int)kie::align_up((size_t)rows, 4);
-  pl->out_rope = pl->out_res + (int)kie::align_up((size_t)2 * max_rows_per_cta(d, n_cta), 4);
-  pl->out_floats = pl->out_rope + dh;
+  pl->out_rope = pl->out_res + (int)kie::align_up((size_t)2 * rows_d, 4);
+  pl->out_moe = pl->out_rope + (int)kie::align_up((size_t)dh, 4);
+  pl->out_floats = moe ? pl->out_moe + kie::MOE_SEL_FLOATS + topk * (rows_gu + rows_d) : pl->out_rope + dh;
   const size_t fixed = kie::smem_bytes(0, pl->vec_floats, pl->out_floats);
   const long long room = (long long)smem_optin - (long long)fixed - 1024;
   int nslot = room > 0 ? (int)(room / (kie::SLOT_BYTES + 16)) : 0;
@@ -96,14 +113,27 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   // weights
   WeightLayout &w = pl->w;
   const size_t qkv = (size_t)(c->n_heads + 2 * c->n_kv_heads) * dh * d * 2;
+  w = WeightLayout{};
   w.qkv = 0;
   w.wo = al(qkv);
-  w.gu = w.wo + al((size_t)d * dq * 2);
-  w.down = w.gu + al((size_t)2 * c->ffn_dim * d * 2);
-  w.layer_stride = w.down + al((size_t)d * c->ffn_dim * 2);
+  if (!moe) {
+    w.gu = w.wo + al((size_t)d * dq * 2);
+    w.down = w.gu + al((size_t)2 * F * d * 2);
+    w.layer_stride = w.down + al((size_t)d * F * 2);
+  } else {
+    w.router = w.wo + al((size_t)d * dq * 2);
+    w.egu = w.router + al((size_t)E * d * 2);
+    w.egu_bytes = al((size_t)2 * F * d);
+    w.edn = w.egu + E * w.egu_bytes;
+    w.edn_bytes = al((size_t)d * F);
+    w.esgu = w.edn + E * w.edn_bytes;
+    w.esdn = w.esgu + al((size_t)E * 2 * F * 4);
+    w.layer_stride = w.esdn + al((size_t)E * d * 4);
+  }
   w.lm = L * w.layer_stride;
   w.embed = w.lm + al((size_t)c->vocab * d * 2);
-  w.total = w.embed + al((size_t)c->vocab * d * 2);
+  w.gffn = w.embed + al((size_t)c->vocab * d * 2);
+  w.total = w.gffn + (moe ? al(L * d * 4) : 0);
   // K/V cache
   pl->kv_bytes = al(L * 2 * c->n_kv_heads * (size_t)c->max_seq * dh * 2);
   // workspace
@@ -119,7 +149,8 @@ const char *make_plan(const kie_config *c, int n_cta, int smem_optin, Plan *pl) 
   s.h = take((size_t)d * 4);
   s.q = take((size_t)dq * 4);
   s.o = take((size_t)dq * 4);
-  s.a = take((size_t)c->ffn_dim * 4);
+  s.a = take((size_t)std::max(F, topk * F) * 4);
+  s.rlog = take((size_t)E * 4);
   s.logits = take((size_t)c->vocab * 4);
   s.part_o = take((size_t)c->n_kv_heads * s.smax * G * dh * 4);
   s.part_ml = take((size_t)c->n_kv_heads * s.smax * G * 2 * 4);
@@ -164,6 +195,7 @@ bool device_info(DeviceInfo *di, std::string *err) {
 
 struct kie_ctx {
   kie_config cfg{};
+  kie_moe_config moe{};  // n_experts == 0: dense FFN
   cudaStream_t stream = nullptr;
   Plan plan{};
   bool owns = false;
@@ -239,9 +271,57 @@ int upload_and_pack(kie_ctx *ctx, const uint16_t *host, int M, int K, uint8_t *d
   return KIE_OK;
 }
 
-int repack_weights(kie_ctx *ctx, const kie_weights *w) {
+int upload(kie_ctx *ctx, uint8_t *dst, const void *host, size_t bytes) {
+  KIE_CUDA(ctx, cudaMemcpyAsync(dst, host, bytes, cudaMemcpyHostToDevice, ctx->stream));
+  return KIE_OK;
+}
+
+// The sparse-MoE FFN of layer l: router as given, each expert's FP8 gate/up (rows interleaved) and down matrices
+// packed through `stage` (>= 2 * F * d bytes), row scales interleaved like the rows, FFN gain as fp32.
+int repack_moe_layer(kie_ctx *ctx, const kie_weights *w, const kie_moe_weights *mw, int l, uint8_t *stage) {
   const kie_config &c = ctx->cfg;
   const Plan &pl = ctx->plan;
+  const int d = c.d_model, F = c.ffn_dim, E = ctx->moe.n_experts;
+  uint8_t *lw = ctx->wbuf + (size_t)l * pl.w.layer_stride;
+  int rc = upload(ctx, lw + pl.w.router, mw->router[l], (size_t)E * d * 2);
+  for (int e = 0; e < E && rc == KIE_OK; ++e) {
+    const size_t m = (size_t)F * d;
+    rc = upload(ctx, stage, mw->gate_q[l] + (size_t)e * m, m);
+    if (rc == KIE_OK) rc = upload(ctx, stage + m, mw->up_q[l] + (size_t)e * m, m);
+    if (rc == KIE_OK) {
+      KIE_CUDA(ctx, kie_launch_pack_fp8(stage, stage + m, lw + pl.w.egu + (size_t)e * pl.w.egu_bytes, 2 * F, d,
+                                        pl.n_cta, ctx->stream));
+      KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+      rc = upload(ctx, stage, mw->down_q[l] + (size_t)e * m, m);
+    }
+    if (rc == KIE_OK) {
+      KIE_CUDA(ctx, kie_launch_pack_fp8(stage, nullptr, lw + pl.w.edn + (size_t)e * pl.w.edn_bytes, d, F, pl.n_cta,
+                                        ctx->stream));
+      KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
+    }
+  }
+  if (rc != KIE_OK) return rc;
+  std::vector<float> sgu((size_t)E * 2 * F), gain(d);
+  for (size_t i = 0; i < (size_t)E * F; ++i) {
+    sgu[2 * i] = mw->gate_s[l][i];
+    sgu[2 * i + 1] = mw->up_s[l][i];
+  }
+  for (int i = 0; i < d; ++i) {
+    __half_raw r;
+    r.x = w->ffn_norm[l][i];
+    gain[i] = __half2float(__half(r));
+  }
+  rc = upload(ctx, lw + pl.w.esgu, sgu.data(), sgu.size() * 4);
+  if (rc == KIE_OK) rc = upload(ctx, lw + pl.w.esdn, mw->down_s[l], (size_t)E * d * 4);
+  if (rc == KIE_OK) rc = upload(ctx, ctx->wbuf + pl.w.gffn + (size_t)l * d * 4, gain.data(), (size_t)d * 4);
+  if (rc == KIE_OK) KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));  // the host vectors die here
+  return rc;
+}
+
+int repack_weights(kie_ctx *ctx, const kie_weights *w, const kie_moe_weights *mw) {
+  const kie_config &c = ctx->cfg;
+  const Plan &pl = ctx->plan;
+  const bool moe = ctx->moe.n_experts > 0;
   const int d = c.d_model, dh = c.head_dim, dq = c.n_heads * dh, F = c.ffn_dim;
   const int Mqkv = (c.n_heads + 2 * c.n_kv_heads) * dh;
   const size_t stage_elems = std::max({(size_t)Mqkv * d, (size_t)d * dq, (size_t)2 * F * d, (size_t)c.vocab * d});
@@ -260,6 +340,10 @@ int repack_weights(kie_ctx *ctx, const kie_weights *w) {
     fuse_qkv(c, w->wq[l], w->wk[l], w->wv[l], host.data());
     rc = upload_and_pack(ctx, host.data(), Mqkv, d, lw + pl.w.qkv, w->attn_norm[l], stage, gain);
     if (rc == KIE_OK) rc = upload_and_pack(ctx, w->wo[l], d, dq, lw + pl.w.wo, nullptr, stage, gain);
+    if (moe) {
+      if (rc == KIE_OK) rc = repack_moe_layer(ctx, w, mw, l, reinterpret_cast<uint8_t *>(stage));
+      continue;
+    }
     if (rc == KIE_OK) {
       fuse_gate_up(c, w->w_gate[l], w->w_up[l], host.data());
       rc = upload_and_pack(ctx, host.data(), 2 * F, d, lw + pl.w.gu, w->ffn_norm[l], stage, gain);
@@ -315,6 +399,17 @@ void fill_base(kie_ctx *ctx) {
   p.out_floats = pl.out_floats;
   p.out_res = pl.out_res;
   p.out_rope = pl.out_rope;
+  p.out_moe = pl.out_moe;
+  p.E = ctx->moe.n_experts;
+  p.top_k = ctx->moe.top_k;
+  p.off_router = (long long)pl.w.router;
+  p.off_egu = (long long)pl.w.egu;
+  p.off_edn = (long long)pl.w.edn;
+  p.off_esgu = (long long)pl.w.esgu;
+  p.off_esdn = (long long)pl.w.esdn;
+  p.egu_bytes = (long long)pl.w.egu_bytes;
+  p.edn_bytes = (long long)pl.w.edn_bytes;
+  p.gffn = (const float *)(ctx->wbuf + pl.w.gffn);
   p.eps = c.rms_eps;
   p.wbase = ctx->wbuf;
   p.layer_stride = (long long)pl.w.layer_stride;
@@ -332,6 +427,7 @@ void fill_base(kie_ctx *ctx) {
   p.q = (float *)(ws + pl.ws.q);
   p.o = (float *)(ws + pl.ws.o);
   p.a = (float *)(ws + pl.ws.a);
+  p.rlog = (float *)(ws + pl.ws.rlog);
   p.logits = (float *)(ws + pl.ws.logits);
   p.part_o = (float *)(ws + pl.ws.part_o);
   p.part_ml = (float *)(ws + pl.ws.part_ml);
@@ -345,25 +441,38 @@ void fill_base(kie_ctx *ctx) {
   p.skip_barrier = -1;
 }
 
-int create_common(const kie_config *cfg, const kie_weights *w, void *stream, void *wdev, size_t wbytes, void *kvdev,
-                  size_t kvbytes, void *wsdev, size_t wsbytes, kie_ctx **out) {
+// moe / mw: null for a dense model.
+int create_common(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w, const kie_moe_weights *mw,
+                  void *stream, void *wdev, size_t wbytes, void *kvdev, size_t kvbytes, void *wsdev, size_t wsbytes,
+                  kie_ctx **out) {
   if (!out) return fail(nullptr, KIE_ERR_INVALID, "out is NULL");
   *out = nullptr;
   if (const char *m = check_config(cfg)) return fail(nullptr, KIE_ERR_INVALID, m);
+  if (const char *m = check_moe(cfg, moe)) return fail(nullptr, KIE_ERR_INVALID, m);
+  const bool dense = moe == nullptr;
   if (!w || !w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
-      !w->ffn_norm || !w->w_gate || !w->w_up || !w->w_down)
+      !w->ffn_norm || (dense && (!w->w_gate || !w->w_up || !w->w_down)))
     return fail(nullptr, KIE_ERR_INVALID, "a weight pointer is NULL");
   for (int l = 0; l < cfg->n_layers; ++l)
-    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->ffn_norm[l] || !w->w_gate[l] ||
-        !w->w_up[l] || !w->w_down[l])
+    if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->ffn_norm[l] ||
+        (dense && (!w->w_gate[l] || !w->w_up[l] || !w->w_down[l])))
       return fail(nullptr, KIE_ERR_INVALID, "a per-layer weight pointer is NULL");
+  if (!dense) {
+    if (!mw || !mw->router || !mw->gate_q || !mw->up_q || !mw->down_q || !mw->gate_s || !mw->up_s || !mw->down_s)
+      return fail(nullptr, KIE_ERR_INVALID, "a MoE weight pointer is NULL");
+    for (int l = 0; l < cfg->n_layers; ++l)
+      if (!mw->router[l] || !mw->gate_q[l] || !mw->up_q[l] || !mw->down_q[l] || !mw->gate_s[l] || !mw->up_s[l] ||
+          !mw->down_s[l])
+        return fail(nullptr, KIE_ERR_INVALID, "a per-layer MoE weight pointer is NULL");
+  }
   DeviceInfo di;
   std::string err;
   if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
   kie_ctx *ctx = new kie_ctx();
   ctx->cfg = *cfg;
+  if (moe) ctx->moe = *moe;
   ctx->stream = (cudaStream_t)stream;
-  if (const char *m = make_plan(cfg, di.sms, di.smem_optin, &ctx->plan)) {
+  if (const char *m = make_plan(cfg, moe, di.sms, di.smem_optin, &ctx->plan)) {
     delete ctx;
     return fail(nullptr, KIE_ERR_INVALID, m);
   }
@@ -400,7 +509,7 @@ int create_common(const kie_config *cfg, const kie_weights *w, void *stream, voi
   cudaError_t e = cudaMemsetAsync(ctx->kvbuf, 0, pl.kv_bytes, ctx->stream);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->wsbuf, 0, pl.ws.total, ctx->stream);
   if (e != cudaSuccess) rc = cuda_fail(ctx, e, "clearing device buffers");
-  if (rc == KIE_OK) rc = repack_weights(ctx, w);
+  if (rc == KIE_OK) rc = repack_weights(ctx, w, mw);
   if (rc == KIE_OK) rc = upload_rope(ctx);
   if (rc != KIE_OK) {
     g_create_error = ctx->err;
@@ -461,16 +570,17 @@ int finish(kie_ctx *ctx) {
 
 extern "C" {
 
-int kie_query_buffers(const kie_config *cfg, int n_cta, kie_buffer_sizes *out) {
+static int query_buffers(const kie_config *cfg, const kie_moe_config *moe, int n_cta, kie_buffer_sizes *out) {
   if (!out) return KIE_ERR_INVALID;
   if (const char *m = check_config(cfg)) return fail(nullptr, KIE_ERR_INVALID, m);
+  if (const char *m = check_moe(cfg, moe)) return fail(nullptr, KIE_ERR_INVALID, m);
   DeviceInfo di{0, n_cta, 232448};
   std::string err;
   if (n_cta <= 0) {
     if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
   }
   Plan pl;
-  if (const char *m = make_plan(cfg, di.sms, di.smem_optin, &pl)) return fail(nullptr, KIE_ERR_INVALID, m);
+  if (const char *m = make_plan(cfg, moe, di.sms, di.smem_optin, &pl)) return fail(nullptr, KIE_ERR_INVALID, m);
   out->weights_bytes = pl.w.total;
   out->kv_bytes = pl.kv_bytes;
   out->workspace_bytes = pl.ws.total;
@@ -478,16 +588,41 @@ int kie_query_buffers(const kie_config *cfg, int n_cta, kie_buffer_sizes *out) {
   return KIE_OK;
 }
 
+int kie_query_buffers(const kie_config *cfg, int n_cta, kie_buffer_sizes *out) {
+  return query_buffers(cfg, nullptr, n_cta, out);
+}
+
+int kie_query_buffers_moe(const kie_config *cfg, const kie_moe_config *moe, int n_cta, kie_buffer_sizes *out) {
+  if (!moe) return fail(nullptr, KIE_ERR_INVALID, "moe is NULL");
+  return query_buffers(cfg, moe, n_cta, out);
+}
+
 int kie_create(const kie_config *cfg, const kie_weights *w, void *stream, kie_ctx **out) {
-  return create_common(cfg, w, stream, nullptr, 0, nullptr, 0, nullptr, 0, out);
+  return create_common(cfg, nullptr, w, nullptr, stream, nullptr, 0, nullptr, 0, nullptr, 0, out);
+}
+
+int kie_create_moe(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w, const kie_moe_weights *mw,
+                   void *stream, kie_ctx **out) {
+  if (!moe) return fail(nullptr, KIE_ERR_INVALID, "moe is NULL");
+  return create_common(cfg, moe, w, mw, stream, nullptr, 0, nullptr, 0, nullptr, 0, out);
+}
+
+int kie_create_moe_with_buffers(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w,
+                                const kie_moe_weights *mw, void *stream, void *weights_dev, size_t weights_bytes,
+                                void *kv_dev, size_t kv_bytes, void *workspace_dev, size_t workspace_bytes,
+                                kie_ctx **out) {
+  if (!moe) return fail(nullptr, KIE_ERR_INVALID, "moe is NULL");
+  if (!weights_dev || !kv_dev || !workspace_dev) return fail(nullptr, KIE_ERR_INVALID, "a device buffer is NULL");
+  return create_common(cfg, moe, w, mw, stream, weights_dev, weights_bytes, kv_dev, kv_bytes, workspace_dev,
+                       workspace_bytes, out);
 }
 
 int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *stream, void *weights_dev,
                             size_t weights_bytes, void *kv_dev, size_t kv_bytes, void *workspace_dev,
                             size_t workspace_bytes, kie_ctx **out) {
   if (!weights_dev || !kv_dev || !workspace_dev) return fail(nullptr, KIE_ERR_INVALID, "a device buffer is NULL");
-  return create_common(cfg, w, stream, weights_dev, weights_bytes, kv_dev, kv_bytes, workspace_dev, workspace_bytes,
-                       out);
+  return create_common(cfg, nullptr, w, nullptr, stream, weights_dev, weights_bytes, kv_dev, kv_bytes, workspace_dev,
+                       workspace_bytes, out);
 }
 
 int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
@@ -499,6 +634,14 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
   std::memcpy(ctx->pinned, tokens, (size_t)n * 4);
   int *tin = (int *)(ctx->wsbuf + ctx->plan.ws.tok_in);
   KIE_CUDA(ctx, cudaMemcpyAsync(tin, ctx->pinned, (size_t)n * 4, cudaMemcpyHostToDevice, ctx->stream));
+  if (ctx->moe.n_experts > 0) {
+    // sparse MoE: the prompt goes through the decode kernel position by position (each token routes to its own
+    // experts), teacher-forced, with the LM head at the last position only
+    int rc = launch(ctx, n, kie::MODE_FORCED, 1, tin, nullptr, nullptr);
+    if (rc == KIE_OK) rc = finish(ctx);
+    if (rc == KIE_OK) ctx->has_logits = true;
+    return rc;
+  }
   // batched: the prompt moves through each layer in chunks of up to PF_TOKENS tokens (kie_prefill.cu)
   const WsLayout &ws = ctx->plan.ws;
   uint8_t *b = ctx->wsbuf;
@@ -702,6 +845,11 @@ int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, in
   return e == cudaSuccess ? KIE_OK : fail(nullptr, KIE_ERR_CUDA, cudaGetErrorString(e));
 }
 
+int64_t kie_packed_offset_fp8(int M, int K, int n_cta, int r, int c) {
+  if (M < 2 || M % 2 || K < 16 || K % 16 || n_cta < 1 || r < 0 || r >= M || c < 0 || c >= K) return -1;
+  return kie::packed_offset_bw(M, K, n_cta, r, c, kie::FP8_TILE_COLS);
+}
+
 int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c) {
   if (M < 2 || M % 2 || K < 1 || n_cta < 1 || r < 0 || r >= M || c < 0 || c >= K) return -1;
   return kie::packed_offset(M, K, n_cta, r, c);
@@ -734,10 +882,11 @@ void *g_noalloc_addr[NOALLOC_MAX_DEVICES];  // device address of g_noalloc_scrat
 std::mutex g_noalloc_mutex;
 
 struct NoallocLayout {
-  size_t x, h, q, o, a, part_o, part_ml, ctl, total;
+  size_t x, h, q, o, a, rlog, part_o, part_ml, ctl, total;
 };
 
-NoallocLayout noalloc_layout(const kie_config &c, const Plan &pl) {
+NoallocLayout noalloc_layout(const kie_config &c, const kie_moe_config &moe, const Plan &pl) {
+  const int pl_topk = moe.top_k, pl_experts = moe.n_experts;
   const int dq = c.n_heads * c.head_dim, G = c.n_heads / c.n_kv_heads;
   NoallocLayout s;
   size_t o = 0;
@@ -750,7 +899,8 @@ NoallocLayout noalloc_layout(const kie_config &c, const Plan &pl) {
   s.h = take((size_t)c.d_model * 4);
   s.q = take((size_t)dq * 4);
   s.o = take((size_t)dq * 4);
-  s.a = take((size_t)c.ffn_dim * 4);
+  s.a = take((size_t)c.ffn_dim * std::max(1, pl_topk) * 4);
+  s.rlog = take((size_t)pl_experts * 4);
   s.part_o = take((size_t)c.n_kv_heads * pl.ws.smax * G * c.head_dim * 4);
   s.part_ml = take((size_t)c.n_kv_heads * pl.ws.smax * G * 2 * 4);
   s.ctl = take(sizeof(kie::Ctl));
@@ -781,7 +931,7 @@ extern "C" int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev) 
   if (n < 1 || !out_tokens_dev) return fail(ctx, KIE_ERR_INVALID, "decode needs n >= 1 and an output buffer");
   if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
   if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
-  const NoallocLayout lay = noalloc_layout(ctx->cfg, ctx->plan);
+  const NoallocLayout lay = noalloc_layout(ctx->cfg, ctx->moe, ctx->plan);
   if (lay.total > KIE_NOALLOC_SCRATCH_BYTES) {
     char buf[200];
     std::snprintf(buf, sizeof buf,
@@ -798,6 +948,7 @@ extern "C" int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev) 
   p.q = (float *)(scr + lay.q);
   p.o = (float *)(scr + lay.o);
   p.a = (float *)(scr + lay.a);
+  p.rlog = (float *)(scr + lay.rlog);
   p.part_o = (float *)(scr + lay.part_o);
   p.part_ml = (float *)(scr + lay.part_ml);
   p.ctl = (kie::Ctl *)(scr + lay.ctl);

@@ -360,20 +360,116 @@ __device__ __forceinline__ int split_pieces(const DecodeParams &p, int c) {
   return s < p.smax ? s : p.smax;
 }
 
-__device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard &g) {
+// ---- sparse-MoE FFN steps ---------------------------------------------------------------------------------
+//
+// Shared-memory selection area (s.out + p.out_moe): an mbarrier that completes once per (token, layer) when the
+// consumers publish the routed experts, then top_k expert ids and top_k routing weights.
+struct MoeSel {
+  uint64_t *bar;
+  int *ids;
+  float *wts;
+};
+
+__device__ __forceinline__ MoeSel moe_sel(const DecodeParams &p, const Smem &s) {
+  float *b = s.out + p.out_moe;
+  return {reinterpret_cast<uint64_t *>(b), reinterpret_cast<int *>(b + 2), b + 2 + MAX_TOP_K};
+}
+
+// Router logits of u = inv_rms(h) * (g o h) for this CTA's router rows (e = CTA, CTA + n_cta, ...): the staged
+// vector already holds g o h, `inv` is inv_rms(h). Rows are read straight from global memory (prefetched into L2
+// at the start of the layer); a CTA-wide dot product per row, summed in a fixed order.
+__device__ inline void moe_router(const DecodeParams &p, Smem &s, int l, float inv) {
+  const int tid = threadIdx.x;
+  const __half *R = reinterpret_cast<const __half *>(p.wbase + (size_t)l * p.layer_stride + p.off_router);
+  for (int e = blockIdx.x; e < p.E; e += p.n_cta) {
+    float acc = 0.f;
+    for (int k = tid * 8; k < p.d; k += NCT * 8) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(R + (size_t)e * p.d + k));
+      acc += dot8(raw, *reinterpret_cast<const float4 *>(s.vec + k), *reinterpret_cast<const float4 *>(s.vec + k + 4));
+    }
+    acc = warp_sum(acc);
+    if ((tid & 31) == 0) s.red[tid >> 5] = acc;
+    consumer_sync();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < NCW; ++w) t += s.red[w];
+      p.rlog[e] = t * inv;
+    }
+    consumer_sync();
+  }
+}
+
+// Every CTA, after the router barrier: the top_k largest logits (the lowest id first among equal ones), in
+// descending order, and the softmax over them; warp 0 computes it (all CTAs get identical results from identical
+// inputs), publishes it to the producer through the selection mbarrier, and every consumer sees it after the
+// closing consumer_sync.
+__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < 32) {
+    constexpr int PER = MAX_EXPERTS / 32;
+    unsigned long long key[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      key[i] = e < p.E ? argmax_key(__ldcg(p.rlog + e), e) : 0ull;
+    }
+    int mine = 0;
+    for (int j = 0; j < p.top_k; ++j) {
+      unsigned long long b = 0ull;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) b = key[i] > b ? key[i] : b;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+        b = other > b ? other : b;
+      }
+      const int id = key_index(b);
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+        if (lane + 32 * i == id) key[i] = 0ull;
+      if (lane == j) mine = id;
+    }
+    const float v = lane < p.top_k ? __ldcg(p.rlog + mine) : -INFINITY;
+    const float mx = warp_max(v);
+    const float ev = lane < p.top_k ? expf(v - mx) : 0.f;
+    const float sum = warp_sum(ev);
+    if (lane < p.top_k) {
+      sel.ids[lane] = mine;
+      sel.wts[lane] = ev / sum;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(sel.bar);
+  }
+  consumer_sync();
+}
+
+__device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard &g, bool moe) {
   const uint64_t policy = l2_evict_first_policy();
   RingPos rp{0, 0u, 0};
   const RowRange rq = rows_of_cta((p.Hq + 2 * p.Hkv) * p.dh, p.n_cta, blockIdx.x);
   const RowRange ro = rows_of_cta(p.d, p.n_cta, blockIdx.x);
-  const RowRange rg = rows_of_cta(2 * p.F, p.n_cta, blockIdx.x);
+  const RowRange rg = rows_of_cta(2 * p.F, p.n_cta, blockIdx.x);  // gate/up rows (of each expert, for MoE)
   const RowRange rl = rows_of_cta(p.V, p.n_cta, blockIdx.x);
   const int dq = p.Hq * p.dh;
+  const MoeSel sel = moe_sel(p, s);
+  uint32_t nsel = 0;  // selections consumed so far (completions of the selection mbarrier)
   bool ok = true;
   for (int t = 0; t < p.n && ok; ++t) {
     for (int l = 0; l < p.L && ok; ++l) {
       const uint8_t *lw = p.wbase + (size_t)l * p.layer_stride;
       ok = ok && produce_region(lw + p.off_qkv + (size_t)rq.r0 * p.d * 2, rq.r1 - rq.r0, p.d, s, p.nslot, rp, policy, g);
       ok = ok && produce_region(lw + p.off_wo + (size_t)ro.r0 * dq * 2, ro.r1 - ro.r0, dq, s, p.nslot, rp, policy, g);
+      if (moe) {
+        // the routed experts are known only once the router has run: wait for the consumers' selection
+        ok = ok && wait_mbar(sel.bar, nsel++ & 1u, g);
+        for (int j = 0; j < p.top_k && ok; ++j)
+          ok = produce_region(lw + p.off_egu + (size_t)sel.ids[j] * p.egu_bytes + (size_t)rg.r0 * p.d, rg.r1 - rg.r0,
+                              p.d, s, p.nslot, rp, policy, g, 1, FP8_TILE_COLS);
+        for (int j = 0; j < p.top_k && ok; ++j)
+          ok = produce_region(lw + p.off_edn + (size_t)sel.ids[j] * p.edn_bytes + (size_t)ro.r0 * p.F, ro.r1 - ro.r0,
+                              p.F, s, p.nslot, rp, policy, g, 1, FP8_TILE_COLS);
+        continue;
+      }
       ok = ok && produce_region(lw + p.off_gu + (size_t)rg.r0 * p.d * 2, rg.r1 - rg.r0, p.d, s, p.nslot, rp, policy, g);
       ok = ok && produce_region(lw + p.off_down + (size_t)ro.r0 * p.F * 2, ro.r1 - ro.r0, p.F, s, p.nslot, rp, policy, g);
     }
@@ -383,6 +479,7 @@ __device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard
   drain_ring(s, p.nslot, rp, g);
 }
 
+template <bool MOE>
 __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard &g) {
   const int tid = threadIdx.x;
   const RowRange rq = rows_of_cta((p.Hq + 2 * p.Hkv) * p.dh, p.n_cta, blockIdx.x);
@@ -429,6 +526,9 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
             bulk_prefetch_l2(Vb, (uint32_t)((j1 - j0) * p.dh * 2));
           }
         }
+        if (MOE && tid == 0)  // this CTA's router rows, read once h is known
+          for (int e = blockIdx.x; e < p.E; e += p.n_cta)
+            bulk_prefetch_l2(p.wbase + (size_t)l * p.layer_stride + p.off_router + (size_t)e * p.d * 2, (uint32_t)p.d * 2);
       }
       if (l > 0) ss = stage_f32(s, p.x, p.d, true);
       consume_region(s, p.nslot, rp, rq.r1 - rq.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
@@ -461,6 +561,51 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       consumer_sync();
       for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.h[ro.r0 + i] = hs[i] = xs[i] + s.out[i];
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+
+      if constexpr (MOE) {
+        // [ROUTER] logits of u = inv_rms(h) * (g o h); the staged g o h stays for the experts
+        ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d);
+        const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
+        moe_router(p, s, l, inv);
+        if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+        const MoeSel sel = moe_sel(p, s);
+        moe_select(p, s, sel);
+        // row scales of this CTA's rows of the routed experts, copied while the first tiles are in flight
+        const int Re = rg.r1 - rg.r0, Rd = ro.r1 - ro.r0;
+        float *const scg = s.out + p.out_moe + MOE_SEL_FLOATS, *const scd = scg + p.top_k * Re;
+        {
+          const float *esg = reinterpret_cast<const float *>(p.wbase + (size_t)l * p.layer_stride + p.off_esgu);
+          const float *esd = reinterpret_cast<const float *>(p.wbase + (size_t)l * p.layer_stride + p.off_esdn);
+          for (int i = tid; i < p.top_k * Re; i += NCT)
+            cp_async4(scg + i, esg + (size_t)sel.ids[i / Re] * 2 * p.F + rg.r0 + i % Re);
+          for (int i = tid; i < p.top_k * Rd; i += NCT)
+            cp_async4(scd + i, esd + (size_t)sel.ids[i / Rd] * p.d + ro.r0 + i % Rd);
+        }
+        // [EXPERT GATE/UP] a_j = silu(gate_j) * up_j for each routed expert j, rows interleaved
+        for (int j = 0; j < p.top_k; ++j) consume_region_fp8(s, p.nslot, rp, Re, p.d, s.vec, inv, s.out + j * Re, g);
+        cp_async_wait_all();
+        consumer_sync();
+        for (int i = tid; i < p.top_k * (Re / 2); i += NCT) {
+          const int j = i / (Re / 2), pr = i % (Re / 2);
+          const float gt = s.out[j * Re + 2 * pr] * scg[j * Re + 2 * pr];
+          const float up = s.out[j * Re + 2 * pr + 1] * scg[j * Re + 2 * pr + 1];
+          p.a[(size_t)j * p.F + rg.r0 / 2 + pr] = gt / (1.0f + expf(-gt)) * up;
+        }
+        if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+
+        // [EXPERT DOWN] x = h + sum_j w_j * (Wd_j a_j)
+        stage_f32(s, p.a, p.top_k * p.F, false);
+        for (int j = 0; j < p.top_k; ++j)
+          consume_region_fp8(s, p.nslot, rp, Rd, p.F, s.vec + (size_t)j * p.F, 1.0f, s.out + j * Rd, g);
+        consumer_sync();
+        for (int i = tid; i < Rd; i += NCT) {
+          float acc = 0.f;
+          for (int j = 0; j < p.top_k; ++j) acc += sel.wts[j] * (scd[j * Rd + i] * s.out[j * Rd + i]);
+          p.x[ro.r0 + i] = xs[i] = hs[i] + acc;
+        }
+        if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
+        continue;
+      }
 
       // [GU] a = silu(gate) * up
       ss = stage_f32(s, p.h, p.d, true);
@@ -521,32 +666,40 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
   }
 }
 
+// MOE selects the sparse-MoE FFN (p.E > 0); the dense instantiation carries none of its code.
+template <bool MOE>
 __global__ void __launch_bounds__(BLOCK, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem s = carve_smem(smem_raw, p.nslot, p.vec_floats, p.out_floats);
+  if (MOE && threadIdx.x == 0) mbar_init(moe_sel(p, s).bar, 1);  // made visible by init_ring's fence and sync
   init_ring(s, p.nslot);
   const Guard g{&p.ctl->status, p.timeout_ns};
   if (threadIdx.x >= NCT) {
-    if (threadIdx.x == NCT) producer_main(p, s, g);
+    if (threadIdx.x == NCT) producer_main(p, s, g, MOE);
     return;
   }
-  consumer_main(p, s, g);
+  consumer_main<MOE>(p, s, g);
 }
 
 }  // namespace kie
 
 // Launch helper used by the C ABI (kie_api.cu).
 cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(kie::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const void *fn = p.E > 0 ? (const void *)kie::decode_kernel<true> : (const void *)kie::decode_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&p};
-  return cudaLaunchCooperativeKernel((const void *)kie::decode_kernel, dim3(p.n_cta), dim3(kie::BLOCK), args, smem,
-                                     stream);
+  return cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kie::BLOCK), args, smem, stream);
 }
 
+// Blocks per SM that both instantiations can keep resident with `smem` bytes of dynamic shared memory.
 int kie_decode_max_blocks_per_sm(size_t smem) {
-  int nb = 0;
-  cudaFuncSetAttribute(kie::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kie::decode_kernel, kie::BLOCK, smem) != cudaSuccess) return -1;
-  return nb;
+  int best = 1 << 30;
+  for (const void *fn : {(const void *)kie::decode_kernel<false>, (const void *)kie::decode_kernel<true>}) {
+    int nb = 0;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kie::BLOCK, smem) != cudaSuccess) return -1;
+    best = nb < best ? nb : best;
+  }
+  return best;
 }

@@ -9,6 +9,9 @@ constexpr int MAX_GROUP = 8;         // query heads per KV head supported by the
 constexpr int ATT_SUB = 32;          // positions per online-softmax sub-chunk (one lane each)
 constexpr int MAX_KV_HEADS = 64;
 constexpr int TRACE_CAP = 4096;      // grid barriers whose per-CTA waits are recorded per launch
+constexpr int MAX_EXPERTS = 256;     // sparse-MoE experts per layer supported by the router step
+constexpr int MAX_TOP_K = 8;         // experts per token
+constexpr int MOE_SEL_FLOATS = 32;   // selection area of the row-result region: ids, weights, sequence word
 
 // Zeroed by the host before every launch.
 struct Ctl {
@@ -58,6 +61,16 @@ struct DecodeParams {
   float *out_logits;   // [n][V] device or null
   unsigned long long timeout_ns;
   int skip_cta, skip_barrier;
+  // sparse-MoE FFN (E > 0; E == 0 is the dense FFN above). Per layer: a router [E][d] (fp16, row-major) and E
+  // SwiGLU experts of width F with FP8 E4M3 weights in the packed layout with FP8_TILE_COLS-wide blocks, each
+  // row with an fp32 scale. In the layer block: off_router; off_egu + e * egu_bytes = expert e's gate/up rows
+  // interleaved [2F][d]; off_edn + e * edn_bytes = its down rows [d][F]; off_esgu: scales [E][2F] (interleaved
+  // like the rows); off_esdn: scales [E][d].
+  int E, top_k;
+  int out_moe;  // floats into the row-result area: the selection (MOE_SEL_FLOATS), then the staged row scales
+  long long off_router, off_egu, off_edn, off_esgu, off_esdn, egu_bytes, edn_bytes;
+  const float *gffn;  // [L][d] FFN RMSNorm gains (fp32), applied to the staged vector (FP8 weights keep them out)
+  float *rlog;        // [E] router logits of the current layer
 };
 
 }  // namespace kie

@@ -10,6 +10,7 @@
 // prefetched while attention runs), done here by the GB300's bulk-copy engine.
 #pragma once
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -228,13 +229,14 @@ __device__ __forceinline__ void ring_advance(RingPos &r, int nslot) {
 
 // Producer: stream the tiles of rows [0, R) of one CTA region (R rows of K columns, packed) into the ring.
 // Returns false if it had to give up (status raised).
+// eb: bytes per element (2 for fp16, 1 for FP8), bw: column-block width of the packed layout.
 __device__ inline bool produce_region(const uint8_t *region, int R, int K, Smem &s, int nslot, RingPos &rp,
-                                      uint64_t policy, const Guard &g) {
+                                      uint64_t policy, const Guard &g, int eb = 2, int bw = TILE_COLS) {
   const uint8_t *src = region;
   for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
     const int rows = min(TILE_ROWS, R - g0);
-    for (int k0 = 0; k0 < K; k0 += TILE_COLS) {
-      const uint32_t bytes = (uint32_t)rows * (uint32_t)min(TILE_COLS, K - k0) * 2u;
+    for (int k0 = 0; k0 < K; k0 += bw) {
+      const uint32_t bytes = (uint32_t)rows * (uint32_t)min(bw, K - k0) * (uint32_t)eb;
       if (!wait_mbar(&s.empty[rp.slot], rp.phase ^ 1u, g)) return false;
       mbar_arrive_expect_tx(&s.full[rp.slot], bytes);
       bulk_g2s(s.ring + (size_t)rp.slot * SLOT_BYTES, src, bytes, &s.full[rp.slot], policy);
@@ -391,6 +393,131 @@ static __device__ __noinline__ void consume_region(Smem &s, int nslot, RingPos &
   rp.phase = phase;
 }
 
+// ---- consumer: one FP8 (E4M3) projection -----------------------------------------------------------------
+
+// Sixteen E4M3 codes (one 16-byte chunk of a tile row, column order = byte order) times x[0..16). Each code
+// pair goes through the hardware E4M3x2 -> f16x2 conversion, which is exact (every E4M3 value is an fp16
+// value), then fp32 FMAs.
+__device__ __forceinline__ float dot16_e4m3(const uint4 w, const float4 x0, const float4 x1, const float4 x2,
+                                            const float4 x3) {
+  const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+  const float4 xs[4] = {x0, x1, x2, x3};
+  float a = 0.f, b = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wd[i] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(wd[i] >> 16), __NV_E4M3);
+    const float2 f0 = __half22float2(__half2(lo)), f1 = __half22float2(__half2(hi));
+    a = fmaf(f0.x, xs[i].x, a);
+    a = fmaf(f0.y, xs[i].y, a);
+    b = fmaf(f1.x, xs[i].z, b);
+    b = fmaf(f1.y, xs[i].w, b);
+  }
+  return a + b;
+}
+
+// tile_loop for FP8 tiles: full FP8_TILE_COLS-wide column blocks, one 16-code chunk per lane and row.
+template <int NJ>
+__device__ __forceinline__ void tile_loop_fp8(const uint8_t *ring, uint64_t *full, uint64_t *empty, const float *vec,
+                                              float (&acc)[ROWS_PER_WARP], int nslot, int &slot, uint32_t &phase,
+                                              int k_end, bool &ok, volatile int *flags, const Guard &g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int k0 = 0; k0 < k_end; k0 += FP8_TILE_COLS) {
+    if (ok && !wait_mbar(&full[slot], phase, g)) {
+      ok = false;
+      flags[0] = 1;
+    }
+    uint4 wv[NJ > 0 ? NJ : 1];
+    const uint8_t *t = ring + (size_t)slot * SLOT_BYTES + (size_t)warp * FP8_TILE_COLS + lane * 16;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) wv[j] = *reinterpret_cast<const uint4 *>(t + (size_t)j * NCW * FP8_TILE_COLS);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == nslot) {
+      slot = 0;
+      phase ^= 1u;
+    }
+    if (NJ > 0) {
+      const float4 *xv = reinterpret_cast<const float4 *>(vec + k0 + lane * 16);
+      const float4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) acc[j] += dot16_e4m3(wv[j], x0, x1, x2, x3);
+    }
+  }
+}
+
+// out[i] = scale * sum_k Q[r0 + i][k] * vec[k] over the R rows of this CTA in one packed FP8 region (codes
+// taken at their E4M3 value; the caller applies the row scales). Same tile walk, warp/row ownership and abort
+// behaviour as consume_region; K is a multiple of 16.
+static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingPos &rp, int R, int K,
+                                                       const float *vec, float scale, float *out, const Guard &g) {
+  bool ok = s.flags[0] == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint8_t *const ring = s.ring;
+  uint64_t *const full = s.full, *const empty = s.empty;
+  volatile int *const flags = s.flags;
+  int slot = rp.slot;
+  uint32_t phase = rp.phase;
+  const int kfull = K / FP8_TILE_COLS * FP8_TILE_COLS;
+  for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
+    const int rows = min(TILE_ROWS, R - g0);
+    const int nj = min(ROWS_PER_WARP, (rows - warp + NCW - 1) / NCW);
+    float acc[ROWS_PER_WARP];
+#pragma unroll
+    for (int j = 0; j < ROWS_PER_WARP; ++j) acc[j] = 0.f;
+    switch (nj) {
+      case 4: tile_loop_fp8<4>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+      case 3: tile_loop_fp8<3>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+      case 2: tile_loop_fp8<2>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+      case 1: tile_loop_fp8<1>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+      default: tile_loop_fp8<0>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+    }
+    if (kfull < K) {  // the last, narrower column block (w codes per row, a multiple of 16)
+      const int w = K - kfull;
+      if (ok && !wait_mbar(&full[slot], phase, g)) {
+        ok = false;
+        flags[0] = 1;
+      }
+      const bool active = ok && lane * 16 < w;
+      uint4 wv[ROWS_PER_WARP];
+      if (active) {
+        const uint8_t *tile = ring + (size_t)slot * SLOT_BYTES;
+#pragma unroll
+        for (int j = 0; j < ROWS_PER_WARP; ++j)
+          if (j < nj) wv[j] = *reinterpret_cast<const uint4 *>(tile + (size_t)(warp + NCW * j) * w + lane * 16);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (++slot == nslot) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      if (active) {
+        const float4 *xv = reinterpret_cast<const float4 *>(vec + kfull + lane * 16);
+        const float4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+#pragma unroll
+        for (int j = 0; j < ROWS_PER_WARP; ++j)
+          if (j < nj) acc[j] += dot16_e4m3(wv[j], x0, x1, x2, x3);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < ROWS_PER_WARP; ++j) {
+      if (j < nj) {
+        const float v = warp_sum(acc[j]);
+        if (lane == 0) out[g0 + warp + NCW * j] = v * scale;
+      }
+    }
+  }
+  rp.slot = slot;
+  rp.phase = phase;
+}
+
+// 4-byte asynchronous global -> shared copy (completion: cp_async_wait_all by the issuing thread).
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---- staging the input vector ---------------------------------------------------------------------------
 
 // vec[0..K) = src (fp32, written by other CTAs earlier in the launch: read through L2). If want_ss, returns
@@ -414,6 +541,27 @@ __device__ inline float stage_f32(Smem &s, const float *src, int K, bool want_ss
 #pragma unroll
   for (int w = 0; w < NCW; ++w) t += s.red[w];
   consumer_sync();  // s.red may be reused right after
+  return t;
+}
+
+// vec[0..K) = src * gain (src fp32 written by other CTAs, read through L2; gain read-only) and the CTA-uniform
+// sum of squares of src (the RMSNorm of src with its gain applied to the staged copy). K a multiple of 4.
+__device__ inline float stage_f32_gain(Smem &s, const float *src, const float *gain, int K) {
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  for (int i = tid * 4; i < K; i += NCT * 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
+    const float4 w = __ldg(reinterpret_cast<const float4 *>(gain + i));
+    *reinterpret_cast<float4 *>(s.vec + i) = make_float4(v.x * w.x, v.y * w.y, v.z * w.z, v.w * w.w);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) s.red[tid >> 5] = ss;
+  consumer_sync();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < NCW; ++w) t += s.red[w];
+  consumer_sync();
   return t;
 }
 

@@ -65,7 +65,31 @@ __global__ void pack_kernel(const uint16_t *src, uint16_t *dst, int M, int K, in
   }
 }
 
+// dst = packed(src) for FP8 codes [M, K] (column blocks of FP8_TILE_COLS codes). With b == null row r is
+// a[r]; otherwise rows interleave two [M/2, K] matrices: row 2i = a[i], row 2i + 1 = b[i] (gate/up pairs).
+// One thread moves 16 consecutive codes of one row; K is a multiple of 16.
+__global__ void pack_fp8_kernel(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n) {
+  const long long chunks = (long long)M * (K / 16);
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < chunks;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / (K / 16));
+    const int c = (int)(idx % (K / 16)) * 16;
+    const uint8_t *src = b ? ((r & 1) ? b : a) + (size_t)(r >> 1) * K + c : a + (size_t)r * K + c;
+    *reinterpret_cast<uint4 *>(dst + packed_offset_bw(M, K, n, r, c, FP8_TILE_COLS)) =
+        *reinterpret_cast<const uint4 *>(src);
+  }
+}
+
 }  // namespace kie
+
+cudaError_t kie_launch_pack_fp8(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n_cta,
+                                cudaStream_t stream) {
+  const long long chunks = (long long)M * (K / 16);
+  int blocks = (int)((chunks + 255) / 256);
+  if (blocks > 65535 * 8) blocks = 65535 * 8;
+  kie::pack_fp8_kernel<<<blocks, 256, 0, stream>>>(a, b, dst, M, K, n_cta);
+  return cudaGetLastError();
+}
 
 cudaError_t kie_launch_gemv(const uint8_t *packed, const __half *x, float *y, int M, int K, int n_cta, int nslot,
                             unsigned long long timeout_ns, cudaStream_t stream) {

@@ -41,16 +41,22 @@ KIE_HD int owner_of_row(int M, int n, int r) {
   return i;
 }
 
-// Element offset of W[r][c] in the packed matrix.
-KIE_HD long long packed_offset(int M, int K, int n, int r, int c) {
+// FP8 (one-byte) matrices use column blocks of FP8_TILE_COLS, so a full tile is again SLOT_BYTES.
+constexpr int FP8_TILE_COLS = 2 * TILE_COLS;
+
+// Element offset of W[r][c] in the packed matrix whose column blocks are bw columns wide.
+KIE_HD long long packed_offset_bw(int M, int K, int n, int r, int c, int bw) {
   const RowRange rr = rows_of_cta(M, n, owner_of_row(M, n, r));
   const int lr = r - rr.r0;
   const int g = lr / TILE_ROWS;
   const int rows_g = (rr.r1 - rr.r0 - g * TILE_ROWS) < TILE_ROWS ? (rr.r1 - rr.r0 - g * TILE_ROWS) : TILE_ROWS;
-  const int b = c / TILE_COLS;
-  const int w = (K - b * TILE_COLS) < TILE_COLS ? (K - b * TILE_COLS) : TILE_COLS;
-  return (long long)rr.r0 * K + (long long)g * TILE_ROWS * K + (long long)rows_g * TILE_COLS * b +
-         (long long)(lr - g * TILE_ROWS) * w + (c - b * TILE_COLS);
+  const int b = c / bw;
+  const int w = (K - b * bw) < bw ? (K - b * bw) : bw;
+  return (long long)rr.r0 * K + (long long)g * TILE_ROWS * K + (long long)rows_g * bw * b +
+         (long long)(lr - g * TILE_ROWS) * w + (c - b * bw);
 }
+
+// Element offset of W[r][c] in a packed fp16 matrix (column blocks of TILE_COLS).
+KIE_HD long long packed_offset(int M, int K, int n, int r, int c) { return packed_offset_bw(M, K, n, r, c, TILE_COLS); }
 
 }  // namespace kie

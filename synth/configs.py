@@ -87,7 +87,7 @@ TWO_B = ModelConfig("llama2b", n_layers=25, d_model=2560, n_heads=20, n_kv_heads
 MOE_M = MoEConfig("moe", n_layers=24, d_model=2048, n_heads=16, n_kv_heads=4, head_dim=128, ffn_dim=1024,
                   vocab=32000, seed=2, n_experts=64, top_k=4, expert_ffn=1024)
 MOE_TINY = MoEConfig("moe_tiny", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=128,
-                     vocab=4096, seed=3, n_experts=8, top_k=4, expert_ffn=128)
+                     vocab=4096, seed=3, gain_std=0.01, n_experts=8, top_k=4, expert_ffn=128)
 
 TINY_DECODE = Workload("tiny_p16_n32", TINY, prompt_len=16, decode_len=32)
 TWO_B_DECODE = Workload("llama2b_p128_n1024", TWO_B, prompt_len=128, decode_len=1024)

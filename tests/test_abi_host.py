@@ -7,7 +7,7 @@ import numpy as np
 import pytest
 
 import persistent_monokernel_decode_gb300 as kie
-from synth.configs import TINY, TWO_B
+from synth.configs import MOE_M, MOE_TINY, TINY, TWO_B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -52,6 +52,57 @@ def test_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
                 tile = block[g0:g0 + rows, k0:k0 + w]
                 # one row-major run of rows*w elements
                 assert np.array_equal(tile.ravel() - tile.min(), np.arange(rows * w))
+
+
+@pytest.mark.parametrize("M,K,n", [(2, 16, 1), (256, 256, 152), (256, 128, 152), (34, 784, 3), (66, 528, 5),
+                                   (100, 1040, 7), (2048, 1024, 152)])
+def test_fp8_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
+    """FP8 expert matrices: one-byte codes in 512-code column blocks, so a full 32-row tile is again 16 KB."""
+    off = np.array([[kie.packed_offset_fp8(M, K, n, r, c) for c in range(K)] for r in range(M)], dtype=np.int64)
+    assert np.array_equal(np.sort(off.ravel()), np.arange(M * K))
+    for cta in range(n):
+        r0, r1 = kie.rows_of_cta(M, n, cta)
+        if r1 == r0:
+            continue
+        block = off[r0:r1]
+        assert block.min() == r0 * K and block.max() == r1 * K - 1
+        for g0 in range(0, r1 - r0, 32):
+            rows = min(32, r1 - r0 - g0)
+            for k0 in range(0, K, 512):
+                w = min(512, K - k0)
+                tile = block[g0:g0 + rows, k0:k0 + w]
+                assert np.array_equal(tile.ravel() - tile.min(), np.arange(rows * w))
+                assert tile.min() % 16 == 0 and (rows * w) % 16 == 0  # a legal bulk copy
+    assert kie.packed_offset_fp8(M, K + 8, n, 0, 0) == -1  # K must be a multiple of 16
+
+
+def test_moe_buffer_plan_without_a_device():
+    cfg = kie.make_config(MOE_M, 768)
+    s = kie.kie_query_buffers(cfg, 152, kie.make_moe_config(MOE_M))
+    E, d, F, L = MOE_M.n_experts, MOE_M.d_model, MOE_M.expert_ffn, MOE_M.n_layers
+    assert s.weights_bytes >= L * E * 3 * F * d  # every expert of every layer is resident
+    assert s.weights_bytes < L * E * 3 * F * d * 1.1 + (2 << 30)
+    assert s.kv_bytes >= MOE_M.kv_bytes_per_token(768)
+    dense = kie.kie_query_buffers(kie.make_config(MOE_TINY, 64), 152)
+    sparse = kie.kie_query_buffers(kie.make_config(MOE_TINY, 64), 152, kie.make_moe_config(MOE_TINY))
+    assert sparse.weights_bytes > dense.weights_bytes
+
+
+@pytest.mark.parametrize("field,value", [("n_experts", 0), ("n_experts", 257), ("top_k", 0), ("top_k", 9)])
+def test_unsupported_moe_configs_are_rejected(field, value):
+    moe = kie.make_moe_config(MOE_TINY)
+    setattr(moe, field, value)
+    with pytest.raises(kie.KieError) as e:
+        kie.kie_query_buffers(kie.make_config(MOE_TINY, 64), 152, moe)
+    assert e.value.code == kie.KIE_ERR_INVALID
+    cfg = kie.make_config(MOE_TINY, 64)
+    cfg.d_model = 264  # a multiple of 8 but not of 16
+    with pytest.raises(kie.KieError):
+        kie.kie_query_buffers(cfg, 152, kie.make_moe_config(MOE_TINY))
+    moe = kie.make_moe_config(MOE_TINY)
+    moe.top_k = moe.n_experts + 1 if moe.n_experts < 8 else 9
+    with pytest.raises(kie.KieError):
+        kie.kie_query_buffers(kie.make_config(MOE_TINY, 64), 152, moe)
 
 
 @pytest.mark.parametrize("M,n", [(2, 1), (2, 152), (256, 152), (3584, 152), (15360, 152), (32000, 152), (10, 3)])

@@ -1,0 +1,195 @@
+"""GPU parity of the sparse-MoE decode (router, top-k softmax, FP8 E4M3 experts with row scales) against the
+oracle's MoE FFN, through the C ABI.
+
+Same bar as the dense model: logits max |diff| <= 2e-2, greedy tokens identical wherever the oracle's top-1/top-2
+margin exceeds 2e-2, teacher forcing so one permitted divergence cannot cascade. The expert selection is itself a
+floating-point decision (a top-k over router logits) that the two sides take from logits rounded differently: where
+the oracle's routing margin (its k-th router logit minus the best unselected one, over every layer of a forward) is
+below ROUTE_EPS, either selection is a correct result and that step's logits are exempt from the bound; the test
+requires most steps to be compared. ROUTE_EPS = 1e-3 against router logits of standard deviation ~0.9 and a
+GPU/oracle hidden-state discrepancy of ~1e-4 relative (fp16 RMSNorm-gain folds, fp32 summation order) leaves a
+factor of ten.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.configs import MOE_DECODE, MOE_M, MOE_TINY
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL = 2e-2
+MARGIN = 2e-2
+ROUTE_EPS = 1e-3
+
+
+@pytest.fixture(scope="module")
+def kie():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import persistent_monokernel_decode_gb300 as k
+    k.build()
+    return k
+
+
+def margins(logits):
+    s = np.sort(logits, axis=-1)
+    return s[..., -1] - s[..., -2]
+
+
+def oracle_run(cfg, w, prompt, n, max_seq):
+    """Greedy oracle decode (fp32) with the routing margin of every forward: route[0] is the last prompt
+    position's, route[i + 1] that of decode step i."""
+    m = oracle.Model(cfg, w, max_seq, 32)
+    m.prefill(prompt[:-1])
+    m.route_margin()
+    cur = m.forward(int(prompt[-1]))
+    route, logits, toks = [m.route_margin()], [cur], []
+    for _ in range(n):
+        toks.append(oracle.argmax(cur))
+        cur = m.forward(toks[-1])
+        logits.append(cur)
+        route.append(m.route_margin())
+    return np.array(toks, dtype=np.int32), np.stack(logits), np.array(route)
+
+
+def check_run(dec, cfg, w, prompt, n, max_seq, min_compared=None):
+    ref_tokens, ref_logits, route = oracle_run(cfg, w, prompt, n, max_seq)
+    settled = route >= ROUTE_EPS  # forwards whose routing rounding cannot change
+    dec.reset()
+    dec.prefill(prompt)
+    err = float(np.max(np.abs(dec.logits() - ref_logits[0])))
+    assert err <= LOGIT_TOL or not settled[0], f"prefill logits differ by {err}"
+    toks, logits = dec.decode_forced(ref_tokens)
+    diff = np.max(np.abs(logits - ref_logits[1:]), axis=1)
+    cmp = settled[1:]
+    assert diff[cmp].max(initial=0.0) <= LOGIT_TOL, f"logits differ by {diff} (routing margins {route})"
+    assert cmp.sum() >= (n if min_compared is None else min_compared), f"routing margins {route}"
+    sure = (margins(ref_logits[:-1]) > MARGIN) & settled[:-1]
+    assert np.array_equal(toks[sure], ref_tokens[sure])
+    return ref_tokens, ref_logits
+
+
+@pytest.fixture(scope="module")
+def tiny(kie):
+    w = synth.moe_weights(MOE_TINY)
+    dec = kie.Decoder(MOE_TINY, w, max_seq=64)
+    yield w, dec
+    dec.close()
+
+
+def test_moe_tiny_teacher_forced_parity(tiny):
+    w, dec = tiny
+    check_run(dec, MOE_TINY, w, synth.tokens(MOE_TINY.seed, 12, MOE_TINY.vocab), 24, 64)
+
+
+def test_moe_tiny_free_running_greedy_matches_until_a_close_call(tiny):
+    w, dec = tiny
+    prompt = synth.tokens(MOE_TINY.seed, 12, MOE_TINY.vocab)
+    ref_tokens, ref_logits, route = oracle_run(MOE_TINY, w, prompt, 24, 64)
+    dec.reset()
+    dec.prefill(prompt)
+    toks = dec.decode(24)
+    close = (margins(ref_logits[:-1]) <= MARGIN) | (route[:-1] < ROUTE_EPS)
+    first_close = int(np.argmax(close)) if np.any(close) else 24
+    assert np.array_equal(toks[:first_close], ref_tokens[:first_close])
+    assert dec.position == 36
+
+
+def test_moe_tiny_split_calls_and_prefill_pieces_are_exact(tiny):
+    _, dec = tiny
+    prompt = synth.tokens(MOE_TINY.seed, 12, MOE_TINY.vocab)
+    dec.reset()
+    dec.prefill(prompt)
+    a = dec.logits()
+    whole = dec.decode(20)
+    dec.reset()
+    dec.prefill(prompt[:5])
+    dec.prefill(prompt[5:6])
+    dec.prefill(prompt[6:])
+    assert np.array_equal(dec.logits(), a)
+    parts = np.concatenate([dec.decode(7), dec.decode(1), dec.decode(12)])
+    assert np.array_equal(whole, parts)
+    st = dec.barrier_stats()
+    assert st["barriers"] == 12 * (6 * MOE_TINY.n_layers + 1)  # 6 grid phases per MoE layer, + the LM head
+
+
+def test_moe_joint_expert_permutation_leaves_the_logits_bit_identical(kie):
+    """Renumbering the experts (router rows and expert matrices together) selects the same experts in the same
+    order, so every CUDA-side sum is taken in the same order: the logits must not change by a single bit."""
+    w = synth.moe_weights(MOE_TINY)
+    prompt = synth.tokens(MOE_TINY.seed, 6, MOE_TINY.vocab)
+    forced = synth.tokens(MOE_TINY.seed + 1, 5, MOE_TINY.vocab)
+    dec = kie.Decoder(MOE_TINY, w, max_seq=32)
+    dec.prefill(prompt)
+    _, before = dec.decode_forced(forced)
+    dec.close()
+    perm = np.random.default_rng(7).permutation(MOE_TINY.n_experts)
+    for lay in w["layers"]:
+        for k in ("router", "gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s"):
+            lay[k] = np.ascontiguousarray(lay[k][perm])
+    dec = kie.Decoder(MOE_TINY, w, max_seq=32)
+    dec.prefill(prompt)
+    _, after = dec.decode_forced(forced)
+    dec.close()
+    assert np.array_equal(before, after)
+
+
+# structure variants: one routed expert (weight exactly 1), every expert routed, several router logits per
+# lane (40 experts), the largest router (256 experts), and widths with full and ragged 512-code FP8 blocks
+MOE_VARIANTS = {
+    "top1": dict(top_k=1),
+    "all_experts": dict(top_k=8),
+    "e40_k3": dict(n_experts=40, top_k=3),
+    "e256_k8": dict(n_experts=256, top_k=8, n_layers=1),
+    "wide_ragged": dict(d_model=784, ffn_dim=528, expert_ffn=528, top_k=2, n_layers=1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MOE_VARIANTS))
+def test_moe_structure_variants(kie, name):
+    cfg = dataclasses.replace(MOE_TINY, name="moe_" + name, **MOE_VARIANTS[name])
+    w = synth.moe_weights(cfg)
+    dec = kie.Decoder(cfg, w, max_seq=40)
+    try:
+        check_run(dec, cfg, w, synth.tokens(cfg.seed, 9, cfg.vocab), 8, 40)
+    finally:
+        dec.close()
+
+
+# ---- the MoE workload at full size (64 experts of width 1,024, top 4, 24 layers), bench launch shape ------
+
+@pytest.fixture(scope="module")
+def moe_m(kie):
+    w = synth.moe_weights(MOE_M)
+    dec = kie.Decoder(MOE_M, w, max_seq=MOE_DECODE.capacity)
+    yield w, dec
+    dec.close()
+
+
+def test_moe_m_sampled_steps_match_oracle(moe_m):
+    """The bench workload's 256-token prompt and the first 16 teacher-forced decode steps, against the oracle (a
+    forward routes 24 x 4 times among 64 experts: about a fifth of them hold a near-tie below ROUTE_EPS)."""
+    w, dec = moe_m
+    check_run(dec, MOE_M, w, synth.prompt(MOE_DECODE), 16, MOE_DECODE.capacity, min_compared=8)
+
+
+def test_moe_m_full_decode_properties(moe_m):
+    """All 512 greedy tokens of the bench workload: valid ids, positions, identical tokens when split."""
+    _, dec = moe_m
+    n = MOE_DECODE.decode_len
+    prompt = synth.prompt(MOE_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    whole = dec.decode(n)
+    assert whole.min() >= 0 and whole.max() < MOE_M.vocab
+    assert dec.position == len(prompt) + n
+    dec.reset()
+    dec.prefill(prompt)
+    parts = np.concatenate([dec.decode(200), dec.decode(n - 200)])
+    assert np.array_equal(whole, parts)
+    assert dec.barrier_stats()["barriers"] == (n - 200) * (6 * MOE_M.n_layers + 1)

@@ -114,7 +114,10 @@ def test_moe_ffn_uses_the_routed_experts_with_their_softmax_weights():
     col = np.array([0.0, 0.75, -0.5, 0.25, 0.5, -0.25, 1.0, -1.0], dtype=np.float16)
     lay["router"] = np.zeros_like(lay["router"])
     lay["router"][:, 0] = col.view(np.uint16)
-    got = oracle.Model(cfg, w, 8, 64).moe_ffn(0, u)
+    m = oracle.Model(cfg, w, 8, 64)
+    got = m.moe_ffn(0, u)
+    # the routing margin: 4th selected logit (0.25) minus the best unselected one (0.0)
+    assert m.route_margin() == 0.25 and m.route_margin() == np.inf
     sel = [6, 1, 4, 3]
     wts = scipy_special.softmax(col.astype(np.float64)[sel])
     ref = sum(wt * _swiglu_expert(lay, e, u) for wt, e in zip(wts, sel))
