@@ -37,14 +37,16 @@ size_t al(size_t v) { return kie::align_up(v, ALIGN); }
 // Byte offsets of the device weight buffer. Per layer (layer_stride apart): qkv, wo, then the dense FFN (gu,
 // down) or the sparse-MoE FFN (router, egu/edn: n_experts packed FP8 matrices egu_bytes/edn_bytes apart,
 // esgu/esdn: their row scales). Then the LM head, the embedding and (MoE) the fp32 FFN gains [L][d].
+// Dense models also keep each layer's four projections as canonical tensor-core tiles for the batched prefill
+// (tc, tc_layer_stride apart, tc_off[QKV, WO, GU, DOWN] within a layer).
 struct WeightLayout {
-  size_t qkv, wo, gu, down, router, egu, edn, esgu, esdn, egu_bytes, edn_bytes, layer_stride, lm, embed, gffn, total;
+  size_t qkv, wo, gu, down, router, egu, edn, esgu, esdn, egu_bytes, edn_bytes, layer_stride, lm, embed, gffn, tc,
+      tc_layer_stride, tc_off[4], total;
 };
 
 struct WsLayout {
   size_t x, h, q, o, a, rlog, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
-      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, total;
-  int pf_part_rows;
+      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, pf_tcb, total;
   int smax;
 };
 
@@ -133,7 +135,18 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   w.lm = L * w.layer_stride;
   w.embed = w.lm + al((size_t)c->vocab * d * 2);
   w.gffn = w.embed + al((size_t)c->vocab * d * 2);
-  w.total = w.gffn + (moe ? al(L * d * 4) : 0);
+  w.tc = w.gffn + (moe ? al(L * d * 4) : 0);
+  const int qkv_rows = (c->n_heads + 2 * c->n_kv_heads) * dh;
+  const int tcM[4] = {qkv_rows, d, 2 * F, d}, tcK[4] = {d, dq, d, F};
+  if (!moe) {
+    size_t o = 0;
+    for (int j = 0; j < 4; ++j) {
+      w.tc_off[j] = o;
+      o += al(kie::kie_tc_tile_bytes(tcM[j], tcK[j]));
+    }
+    w.tc_layer_stride = o;
+  }
+  w.total = w.tc + L * w.tc_layer_stride;
   // K/V cache
   pl->kv_bytes = al(L * 2 * c->n_kv_heads * (size_t)c->max_seq * dh * 2);
   // workspace
@@ -170,8 +183,15 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   s.pf_o = take((size_t)kie::PF_TOKENS * dq * 4);
   s.pf_a = take((size_t)kie::PF_TOKENS * c->ffn_dim * 4);
   s.pf_scale = take((size_t)kie::PF_TOKENS * 4);
-  s.pf_part_rows = std::max((c->n_heads + 2 * c->n_kv_heads) * dh, d);  // the projections that may be split
-  s.pf_part = take((size_t)kie::PF_PART_SLICES * kie::PF_TOKENS * s.pf_part_rows * 4);
+  size_t part_rows = 0, kt_max = 0;  // the K splits of each tensor-core projection, side by side
+  for (int j = 0; j < 4 && !moe; ++j) {
+    int kps, ns;
+    kie::kie_tc_splits((tcM[j] + 127) / 128, (tcK[j] + 63) / 64, n_cta, &kps, &ns);
+    part_rows = std::max(part_rows, (size_t)ns * tcM[j]);
+    kt_max = std::max(kt_max, (size_t)(tcK[j] + 63) / 64);
+  }
+  s.pf_part = take((size_t)kie::PF_TOKENS * part_rows * 4);
+  s.pf_tcb = take(kt_max * 2 * kie::PF_TOKENS * 64 * 2);
   s.total = o;
   return nullptr;
 }
@@ -257,8 +277,10 @@ void fuse_gate_up(const kie_config &c, const uint16_t *wg, const uint16_t *wu, u
   }
 }
 
+// Upload a row-major fp16 [M, K] matrix and pack it for the decode (dst) and, if tc_dst is not null, as
+// canonical tensor-core tiles for the prefill; gain_host (or null) is folded into the columns of both.
 int upload_and_pack(kie_ctx *ctx, const uint16_t *host, int M, int K, uint8_t *dst, const uint16_t *gain_host,
-                    uint16_t *stage, uint16_t *gain_dev) {
+                    uint16_t *stage, uint16_t *gain_dev, uint8_t *tc_dst = nullptr) {
   const size_t bytes = (size_t)M * K * 2;
   KIE_CUDA(ctx, cudaMemcpyAsync(stage, host, bytes, cudaMemcpyHostToDevice, ctx->stream));
   const uint16_t *g = nullptr;
@@ -267,6 +289,7 @@ int upload_and_pack(kie_ctx *ctx, const uint16_t *host, int M, int K, uint8_t *d
     g = gain_dev;
   }
   KIE_CUDA(ctx, kie_launch_pack(stage, (uint16_t *)dst, M, K, ctx->plan.n_cta, g, ctx->stream));
+  if (tc_dst) KIE_CUDA(ctx, kie_launch_tc_pack(stage, M, K, g, tc_dst, ctx->stream));
   KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
   return KIE_OK;
 }
@@ -337,18 +360,22 @@ int repack_weights(kie_ctx *ctx, const kie_weights *w, const kie_moe_weights *mw
   int rc = KIE_OK;
   for (int l = 0; l < c.n_layers && rc == KIE_OK; ++l) {
     uint8_t *lw = ctx->wbuf + (size_t)l * pl.w.layer_stride;
+    uint8_t *tw = moe ? nullptr : ctx->wbuf + pl.w.tc + (size_t)l * pl.w.tc_layer_stride;
     fuse_qkv(c, w->wq[l], w->wk[l], w->wv[l], host.data());
-    rc = upload_and_pack(ctx, host.data(), Mqkv, d, lw + pl.w.qkv, w->attn_norm[l], stage, gain);
-    if (rc == KIE_OK) rc = upload_and_pack(ctx, w->wo[l], d, dq, lw + pl.w.wo, nullptr, stage, gain);
+    rc = upload_and_pack(ctx, host.data(), Mqkv, d, lw + pl.w.qkv, w->attn_norm[l], stage, gain,
+                         tw ? tw + pl.w.tc_off[0] : nullptr);
+    if (rc == KIE_OK)
+      rc = upload_and_pack(ctx, w->wo[l], d, dq, lw + pl.w.wo, nullptr, stage, gain, tw ? tw + pl.w.tc_off[1] : nullptr);
     if (moe) {
       if (rc == KIE_OK) rc = repack_moe_layer(ctx, w, mw, l, reinterpret_cast<uint8_t *>(stage));
       continue;
     }
     if (rc == KIE_OK) {
       fuse_gate_up(c, w->w_gate[l], w->w_up[l], host.data());
-      rc = upload_and_pack(ctx, host.data(), 2 * F, d, lw + pl.w.gu, w->ffn_norm[l], stage, gain);
+      rc = upload_and_pack(ctx, host.data(), 2 * F, d, lw + pl.w.gu, w->ffn_norm[l], stage, gain, tw + pl.w.tc_off[2]);
     }
-    if (rc == KIE_OK) rc = upload_and_pack(ctx, w->w_down[l], d, F, lw + pl.w.down, nullptr, stage, gain);
+    if (rc == KIE_OK)
+      rc = upload_and_pack(ctx, w->w_down[l], d, F, lw + pl.w.down, nullptr, stage, gain, tw + pl.w.tc_off[3]);
   }
   if (rc == KIE_OK) rc = upload_and_pack(ctx, w->lm_head, c.vocab, d, ctx->wbuf + pl.w.lm, w->final_norm, stage, gain);
   if (rc == KIE_OK) {
@@ -644,16 +671,20 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
   }
   // batched: the prompt moves through each layer in chunks of up to PF_TOKENS tokens (kie_prefill.cu)
   const WsLayout &ws = ctx->plan.ws;
+  const WeightLayout &wl = ctx->plan.w;
   uint8_t *b = ctx->wsbuf;
-  const kie::PrefillBufs pb{(float *)(b + ws.pf_x), (float *)(b + ws.pf_h), (float *)(b + ws.pf_q),
-                            (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale),
-                            (float *)(b + ws.pf_part), ws.pf_part_rows};
+  kie::PrefillBufs pb{(float *)(b + ws.pf_x), (float *)(b + ws.pf_h), (float *)(b + ws.pf_q),
+                      (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale),
+                      (float *)(b + ws.pf_part), ctx->wbuf + wl.tc, (long long)wl.tc_layer_stride,
+                      {(long long)wl.tc_off[0], (long long)wl.tc_off[1], (long long)wl.tc_off[2], (long long)wl.tc_off[3]},
+                      b + ws.pf_tcb, &ctx->base.ctl->status, ctx->timeout_ns};
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.ctl, 0, sizeof(kie::Ctl), ctx->stream));
   const cudaError_t e = kie_run_prefill(ctx->base, pb, tin, ctx->pos, n, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
-  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
   ctx->pos += n;
-  ctx->has_logits = true;
-  return KIE_OK;
+  const int rc = finish(ctx);  // the status word: a tensor-core GEMM wait that ran out resets the sequence
+  if (rc == KIE_OK) ctx->has_logits = true;
+  return rc;
 }
 
 int kie_decode_async(kie_ctx *ctx, int n, int32_t *out_tokens_dev) {

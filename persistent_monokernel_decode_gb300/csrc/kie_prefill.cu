@@ -6,17 +6,22 @@
 //
 // Kernels, per chunk of T tokens:
 //   pf_embed  X[t] = fp32(E[tok[t]])
-//   per layer: pf_rms(X) -> pf_gemm QKV (RoPE, K/V append, q) -> pf_attn (causal, over the cache) ->
-//              pf_gemm WO (H = X + Wo o) -> pf_rms(H) -> pf_gemm GU (A = silu(g) u) -> pf_gemm DOWN (X = H + Wd a)
-//   after the last chunk: pf_rms(last X) -> pf_gemm LM head (one token) -> pf_argmax (next token)
-// Every output's sums run in a fixed order that does not depend on how the prompt is cut into chunks, so a
-// prompt prefilled in pieces leaves bit-identical logits and cache.
+//   per layer: pf_rms(X) -> projection QKV (RoPE, K/V append, q) -> pf_attn (causal, over the cache) ->
+//              projection WO (H = X + Wo o) -> pf_rms(H) -> projection GU (A = silu(g) u) -> projection DOWN
+//              (X = H + Wd a)
+//   after the last chunk: pf_rms(last X) -> pf_gemm LM head (one token, CUDA cores) -> pf_argmax (next token)
+// A projection is a tensor-core GEMM (kie_tcgemm.cuh: the chunk's activations split into fp16 high and low
+// parts, tcgen05.mma into TMEM, K split over blocks so that every SM has one) followed by pf_reduce, which adds
+// the K splits in order and applies the epilogue. No sum's order depends on how the prompt is cut into chunks
+// (a token's column of the MMA is computed like any other), so a prompt prefilled in pieces leaves bit-identical
+// logits and cache.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kie_decode.cuh"
 #include "kie_layout.h"
 #include "kie_prefill.cuh"
+#include "kie_tcgemm.cuh"
 
 namespace kie {
 namespace {
@@ -30,7 +35,7 @@ constexpr int XS = PF_TOKENS + 4;  // padded token stride of the staged input (b
 enum Epi { EPI_QKV = 0, EPI_WO = 1, EPI_GU = 2, EPI_DOWN = 3, EPI_LM = 4 };
 
 struct GemmArgs {
-  const uint8_t *w;      // packed projection [M, K] (all CTAs' regions)
+  const uint8_t *w;      // LM head: packed [M, K] (all CTAs' regions)
   int M, K, n_cta;       // rows, columns, CTAs the layout was packed for
   const float *in;       // [T][K] token-major input rows
   const float *scale;    // [T] per-token RMS scale, or null (1)
@@ -41,8 +46,7 @@ struct GemmArgs {
   __half *kv;            // QKV: this layer's K plane base ([2][Hkv][max_seq][dh])
   const float2 *rope;    // QKV: [max_seq][dh/2]
   int pos0, Hq, Hkv, dh, max_seq;
-  // split K: ksplit blocks per row group each sum a contiguous 1/ksplit of the columns into part
-  // ([ksplit][PF_TOKENS][M] raw sums); pf_reduce then adds the slices in order and applies the epilogue
+  // pf_reduce input: the raw sums of ksplit K splits, part[ksplit][PF_TOKENS][M], added in order
   int ksplit;
   float *part;
 };
@@ -98,9 +102,9 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
   const int R = rr.r1 - rr.r0, K = a.K;
   const __half *region = reinterpret_cast<const __half *>(a.w) + (size_t)rr.r0 * K;
   {
-    const int g0 = (int)(blockIdx.y / a.ksplit) * GR, kpart = (int)(blockIdx.y % a.ksplit);
+    const int g0 = (int)blockIdx.y * GR;
     if (g0 >= R) return;
-    const int k_lo = K / a.ksplit * kpart, k_hi = K / a.ksplit * (kpart + 1);
+    const int k_lo = 0, k_hi = K;
     const int rows = min(GR, R - g0);
     const int bw = TILE_COLS;  // the packed layout's column blocks
     const __half *gbase = region + (size_t)g0 * K;
@@ -174,9 +178,7 @@ __global__ void __launch_bounds__(PF_THREADS) pf_gemm(const GemmArgs a) {
         const int lr = g0 + 4 * ty + i;
         if (lr >= R) continue;
         const int r = rr.r0 + lr;
-        if (a.ksplit > 1) {
-          a.part[((size_t)kpart * PF_TOKENS + t) * a.M + r] = acc[i][j];
-        } else if (EPI == EPI_QKV || EPI == EPI_GU) {
+        if (EPI == EPI_QKV || EPI == EPI_GU) {
           if ((i & 1) == 0) epi_pair<EPI>(a, t, r, acc[i][j], acc[i + 1][j]);  // R and g0 even: pairs whole
         } else {
           epi_one<EPI>(a, t, r, acc[i][j]);
@@ -390,22 +392,30 @@ __global__ void pf_argmax(const float *logits, int V, Persist *persist) {
   }
 }
 
-constexpr int KSPLIT_COLS = 1280;  // columns per K slice when a projection is split
-
-// One projection: blocks over (CTA region, row group, K slice). Projections whose regions are a single row
-// group (too few blocks to fill the GPU otherwise) are split into slices of KSPLIT_COLS columns.
-template <int EPI>
-cudaError_t gemm(GemmArgs a, float *part, int part_rows, cudaStream_t st) {
+// The LM head of the last prompt token (a GEMV: T = 1) on the decode's packed weights.
+cudaError_t lm_head(GemmArgs a, cudaStream_t st) {
   const int groups = (2 * ((a.M / 2 + a.n_cta - 1) / a.n_cta) + GR - 1) / GR;  // row groups of the largest region
   a.ksplit = 1;
-  a.part = part;
-  if (groups == 1 && part && a.M <= part_rows && a.K % KSPLIT_COLS == 0 && a.K / KSPLIT_COLS <= PF_PART_SLICES)
-    a.ksplit = a.K / KSPLIT_COLS;
-  pf_gemm<EPI><<<dim3(a.n_cta, groups * a.ksplit), PF_THREADS, 0, st>>>(a);
-  if (a.ksplit > 1) {
-    const long long n = (long long)a.T * ((EPI == EPI_QKV || EPI == EPI_GU) ? a.M / 2 : a.M);
-    pf_reduce<EPI><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
-  }
+  a.part = nullptr;
+  pf_gemm<EPI_LM><<<dim3(a.n_cta, groups), PF_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// One projection of the chunk on the tensor cores: split a.in into hi/lo tiles, the GEMM of the K splits into
+// b.part, then pf_reduce (splits in order + epilogue).
+template <int EPI>
+cudaError_t tc_project(GemmArgs a, const uint8_t *w_tiles, const PrefillBufs &b, cudaStream_t st) {
+  const int KT = (a.K + TC_KT - 1) / TC_KT, Mt = (a.M + TC_M - 1) / TC_M;
+  int kps, ns;
+  kie_tc_splits(Mt, KT, a.n_cta, &kps, &ns);
+  const long long nb = (long long)TC_N * KT * (TC_KT / 8);
+  tc_split_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, st>>>(a.in, a.T, a.K, KT, b.tc_b);
+  const TcArgs t{w_tiles, b.tc_b, KT, kps, b.part, a.M, a.T, b.status, b.timeout_ns};
+  tc_gemm_kernel<<<dim3(Mt, ns), TC_THREADS, TC_SMEM, st>>>(t);
+  a.ksplit = ns;
+  a.part = b.part;
+  const long long n = (long long)a.T * ((EPI == EPI_QKV || EPI == EPI_GU) ? a.M / 2 : a.M);
+  pf_reduce<EPI><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -417,7 +427,8 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
   using namespace kie;
   const int d = p.d, dq = p.Hq * p.dh, F = p.F, qkv = (p.Hq + 2 * p.Hkv) * p.dh;
   const size_t plane = (size_t)p.max_seq * p.dh;
-  cudaError_t e = cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+  if (e != cudaSuccess) return e;
   int last_t = 0;
   for (int c0 = 0; c0 < n; c0 += PF_TOKENS) {
     const int T = n - c0 < PF_TOKENS ? n - c0 : PF_TOKENS, pos = pos0 + c0;
@@ -425,7 +436,7 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
     pf_embed<<<T, 256, 0, st>>>(tok_dev + c0, T, p.embed, d, b.x);
     const int rms_blocks = (T * 32 + 255) / 256;
     for (int l = 0; l < p.L; ++l) {
-      const uint8_t *lw = p.wbase + (size_t)l * p.layer_stride;
+      const uint8_t *tw = b.tc_w + (size_t)l * b.tc_layer_stride;
       __half *kvl = p.kv + (size_t)l * 2 * p.Hkv * plane;
       pf_rms<<<rms_blocks, 256, 0, st>>>(b.x, T, d, p.eps, b.scale);
       GemmArgs a{};
@@ -439,44 +450,40 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.rope = p.rope;
       a.kv = kvl;
       // QKV (+ RoPE, K/V append, q)
-      a.w = lw + p.off_qkv;
       a.M = qkv;
       a.K = d;
       a.in = b.x;
       a.scale = b.scale;
       a.out = b.q;
-      if ((e = gemm<EPI_QKV>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
+      if ((e = tc_project<EPI_QKV>(a, tw + b.tc_off[0], b, st)) != cudaSuccess) return e;
       // attention over positions 0 .. pos0 + t
       const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS);
       if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
       else pf_attn<2><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
       // WO + residual
-      a.w = lw + p.off_wo;
       a.M = d;
       a.K = dq;
       a.in = b.o;
       a.scale = nullptr;
       a.out = b.h;
       a.resid = b.x;
-      if ((e = gemm<EPI_WO>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
+      if ((e = tc_project<EPI_WO>(a, tw + b.tc_off[1], b, st)) != cudaSuccess) return e;
       // gate/up + SwiGLU
       pf_rms<<<rms_blocks, 256, 0, st>>>(b.h, T, d, p.eps, b.scale);
-      a.w = lw + p.off_gu;
       a.M = 2 * F;
       a.K = d;
       a.in = b.h;
       a.scale = b.scale;
       a.out = b.a;
-      if ((e = gemm<EPI_GU>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
+      if ((e = tc_project<EPI_GU>(a, tw + b.tc_off[2], b, st)) != cudaSuccess) return e;
       // down + residual
-      a.w = lw + p.off_down;
       a.M = d;
       a.K = F;
       a.in = b.a;
       a.scale = nullptr;
       a.out = b.x;
       a.resid = b.h;
-      if ((e = gemm<EPI_DOWN>(a, b.part, b.part_rows, st)) != cudaSuccess) return e;
+      if ((e = tc_project<EPI_DOWN>(a, tw + b.tc_off[3], b, st)) != cudaSuccess) return e;
     }
   }
   // logits of the last prompt token and the next token to emit
@@ -491,7 +498,14 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
   a.scale = b.scale;
   a.T = 1;
   a.out = p.logits;
-  if ((e = kie::gemm<kie::EPI_LM>(a, nullptr, 0, st)) != cudaSuccess) return e;
+  if ((e = kie::lm_head(a, st)) != cudaSuccess) return e;
   kie::pf_argmax<<<1, 1024, 0, st>>>(p.logits, p.V, p.persist);
+  return cudaGetLastError();
+}
+
+cudaError_t kie_launch_tc_pack(const uint16_t *src, int M, int K, const uint16_t *gain, uint8_t *dst, cudaStream_t st) {
+  const int KT = (K + kie::TC_KT - 1) / kie::TC_KT, Mp = (M + kie::TC_M - 1) / kie::TC_M * kie::TC_M;
+  const long long n = (long long)Mp * KT * (kie::TC_KT / 8);
+  kie::tc_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, M, K, KT, gain, dst);
   return cudaGetLastError();
 }
