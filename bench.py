@@ -12,6 +12,7 @@ workload. With N > 1 (torchrun) every rank runs an independent replica: the path
 Other modes (not the headline line): --long runs the long-context workload (prompt 8,192, 512 new tokens);
 --moe the sparse-MoE workload (24 layers, 64 FP8 experts of width 1,024, top 4; prompt 256, 512 new tokens),
 whose MBU counts the bytes a token actually streams (attention, router, the 4 routed experts, LM head);
+--prefill N times the batched prefill of an N-token prompt (tensor-core projections, split causal attention);
 --gemv-sweep prints one JSON line per standalone GEMV shape (GB/s, cold HBM); --phase-gemv does the same for
 the decode's five projection shapes of the 2B model (the phase-split view of the weight stream).
 """
@@ -311,6 +312,46 @@ def cpu_baseline_sample(seconds_budget=15.0, max_forwards=400, model=None, weigh
             "sample": f"{n} greedy decode forwards of the {model.name} model after an 8-token prefill ({dt:.1f} s)"}
 
 
+def prefill_bench(args):
+    """kie_prefill of an N-token prompt (reset + prefill, CUDA events on the library's stream): tokens/s and the
+    projections' useful TFLOP/s (2 x parameters x tokens; the attention's FLOP are reported separately)."""
+    import dataclasses
+
+    import torch
+
+    import persistent_monokernel_decode_gb300 as kie
+    import synth
+    from synth.configs import TWO_B
+
+    n = args.prefill
+    model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
+    kie.build()
+    w = synth.model_weights(model)
+    prompt = synth.tokens(model.seed, n, model.vocab)
+    dec = kie.Decoder(model, w, max_seq=n + 16)
+    del w
+    times = []
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(dec.stream)
+        dec.reset()
+        dec.prefill(prompt)
+        e1.record(dec.stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) / 1e3)
+    dec.close()
+    t = sum(times) / len(times)
+    d, dh, F = model.d_model, model.head_dim, model.ffn_dim
+    params = model.n_layers * ((model.n_heads + 2 * model.n_kv_heads) * dh * d + d * model.n_heads * dh + 3 * F * d)
+    att = 4 * model.n_heads * dh * sum(range(1, n + 1)) * model.n_layers
+    print(json.dumps({"metric": "batched prefill tok/s", "value": n / t, "unit": "tok/s", "ms": 1e3 * t,
+                      "steps": args.steps, "warmup": args.warmup, "tokens": n, "layers": model.n_layers,
+                      "projection_tflops_useful": 2 * params * n / t / 1e12, "attention_gflop": att / 1e9}),
+          flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -322,6 +363,8 @@ def main():
     ap.add_argument("--prompt", type=int, default=PROMPT)
     ap.add_argument("--decode", type=int, default=NEW)
     ap.add_argument("--long", action="store_true", help="the long-context workload: prompt 8,192, 512 new tokens")
+    ap.add_argument("--prefill", type=int, default=0, metavar="N",
+                    help="time the batched prefill of an N-token prompt of the 2B model (or --layers of its widths)")
     ap.add_argument("--moe", action="store_true",
                     help="the sparse-MoE workload (64 FP8 experts, top 4): prompt 256, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
@@ -340,6 +383,9 @@ def main():
         gemv_sweep(args, phase_shapes(), "2B decode projection as one standalone GEMV: GB/s (cold HBM, CUDA graph)")
         return
     world, rank, local = dist_setup()
+    if args.prefill:
+        prefill_bench(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

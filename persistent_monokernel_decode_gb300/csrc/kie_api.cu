@@ -46,7 +46,7 @@ struct WeightLayout {
 
 struct WsLayout {
   size_t x, h, q, o, a, rlog, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
-      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, pf_tcb, total;
+      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, pf_tcb, pf_att_o, pf_att_ml, total;
   int smax;
 };
 
@@ -192,6 +192,9 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   }
   s.pf_part = take((size_t)kie::PF_TOKENS * part_rows * 4);
   s.pf_tcb = take(kt_max * 2 * kie::PF_TOKENS * 64 * 2);
+  const size_t att_parts = moe ? 0 : (size_t)kie::kie_pf_att_pieces(c->max_seq) * kie::PF_TOKENS * c->n_heads;
+  s.pf_att_o = take(att_parts * dh * 4);
+  s.pf_att_ml = take(att_parts * 2 * 4);
   s.total = o;
   return nullptr;
 }
@@ -675,7 +678,8 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
   uint8_t *b = ctx->wsbuf;
   kie::PrefillBufs pb{(float *)(b + ws.pf_x), (float *)(b + ws.pf_h), (float *)(b + ws.pf_q),
                       (float *)(b + ws.pf_o), (float *)(b + ws.pf_a), (float *)(b + ws.pf_scale),
-                      (float *)(b + ws.pf_part), ctx->wbuf + wl.tc, (long long)wl.tc_layer_stride,
+                      (float *)(b + ws.pf_part), (float *)(b + ws.pf_att_o), (float *)(b + ws.pf_att_ml),
+                      ctx->wbuf + wl.tc, (long long)wl.tc_layer_stride,
                       {(long long)wl.tc_off[0], (long long)wl.tc_off[1], (long long)wl.tc_off[2], (long long)wl.tc_off[3]},
                       b + ws.pf_tcb, &ctx->base.ctl->status, ctx->timeout_ns};
   KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.ctl, 0, sizeof(kie::Ctl), ctx->stream));

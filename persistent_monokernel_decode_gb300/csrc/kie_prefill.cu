@@ -28,6 +28,7 @@ namespace {
 
 constexpr int PF_THREADS = 256;
 constexpr int PA_WARPS = 4;  // tokens (one warp each) per attention block
+constexpr int PA_PIECE = PF_ATT_PIECE;  // positions per attention piece (fixed boundaries 0, 512, 1024, ...)
 constexpr int GR = TILE_ROWS;    // output rows per block pass (a row group of the packed layout)
 constexpr int KC = 32;           // columns per shared-memory stage
 constexpr int XS = PF_TOKENS + 4;  // padded token stride of the staged input (bank spread)
@@ -223,12 +224,15 @@ __global__ void pf_embed(const int *tok, int T, const __half *E, int d, float *x
   for (int i = threadIdx.x; i < d; i += blockDim.x) x[(size_t)t * d + i] = __half2float(row[i]);
 }
 
-// Causal attention of T new tokens (positions pos0 .. pos0+T-1) over the cache of one layer. Block: one KV head
-// and PA_WARPS consecutive tokens, a warp per token with all G query heads of the group; the 32-position K/V
-// tiles are shared by the block. Scores, online softmax and P.V follow the decode kernel's formulas.
+// Causal attention of T new tokens (positions pos0 .. pos0+T-1) over the cache of one layer. Block: one KV head,
+// PA_WARPS consecutive tokens (a warp per token with all G query heads of the group) and one piece z of the
+// cached positions, [z * PA_PIECE, (z + 1) * PA_PIECE); the 32-position K/V tiles are shared by the block.
+// Scores, online softmax and P.V follow the decode kernel's formulas. A token whose positions fit in one piece
+// writes its output; otherwise every piece writes its partial (m, l, unnormalised o) and pf_attn_merge combines
+// them. Piece boundaries are absolute positions, so a token's arithmetic does not depend on its chunk.
 template <int DPL>
 __global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, int pos0, const __half *kvl, int Hq,
-                                                         int Hkv, int max_seq, float *o) {
+                                                         int Hkv, int max_seq, float *o, float *po, float *pml) {
   constexpr int DH = DPL * 32, U = DH / 8;
   __shared__ __align__(16) __half Ks[32 * DH];
   __shared__ __align__(16) __half Vs[32 * DH];
@@ -239,7 +243,9 @@ __global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, 
   const int t = blockIdx.y * PA_WARPS + warp;
   const bool live = t < T;
   const int pos = pos0 + t;  // this warp's query position
-  const int last = pos0 + min(T, blockIdx.y * PA_WARPS + PA_WARPS) - 1;  // the block's largest position
+  const int z = blockIdx.z, jlo = z * PA_PIECE;
+  const int last = min(pos0 + min(T, (int)blockIdx.y * PA_WARPS + PA_WARPS) - 1, jlo + PA_PIECE - 1);  // block's end
+  if (jlo > last) return;  // no position of this piece is attended by the block's tokens
   const size_t plane = (size_t)max_seq * DH;
   const __half *Kb = kvl + (size_t)kh * plane, *Vb = kvl + (size_t)(Hkv + kh) * plane;
   const float qscale = 1.0f / sqrtf((float)DH);
@@ -268,8 +274,8 @@ __global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, 
       }
     }
   };
-  fetch(0);
-  for (int jb = 0; jb <= last; jb += 32) {
+  fetch(jlo);
+  for (int jb = jlo; jb <= last; jb += 32) {
     __syncthreads();  // the previous tile is no longer read
 #pragma unroll
     for (int k = 0; k < UPT; ++k) {
@@ -357,15 +363,44 @@ __global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, 
     }
     __syncwarp();
   }
-  if (!live) return;
+  if (!live || jlo > pos) return;
+  const bool single = pos < PA_PIECE;  // the token's only piece
 #pragma unroll
   for (int h = 0; h < MAX_GROUP; ++h)
     if (h < G) {
-      const float inv = 1.0f / l[h];
+      const size_t oi = (size_t)t * Hq + (size_t)(kh * G + h);
+      if (single) {
+        const float inv = 1.0f / l[h];
 #pragma unroll
-      for (int e2 = 0; e2 < DPL; ++e2)
-        o[(size_t)t * Hq * DH + (size_t)(kh * G + h) * DH + lane * DPL + e2] = acc[h][e2] * inv;
+        for (int e2 = 0; e2 < DPL; ++e2) o[oi * DH + lane * DPL + e2] = acc[h][e2] * inv;
+      } else {
+        const size_t pi = (size_t)z * T * Hq + oi;
+#pragma unroll
+        for (int e2 = 0; e2 < DPL; ++e2) po[pi * DH + lane * DPL + e2] = acc[h][e2];
+        if (lane == 0) {
+          pml[pi * 2] = m[h];
+          pml[pi * 2 + 1] = l[h];
+        }
+      }
     }
+}
+
+// o of the tokens whose positions span several pieces: pieces in ascending order, w_z = exp(m_z - M),
+// o = sum_z w_z o_z / sum_z w_z l_z. Block: one token and one query head, a thread per dimension.
+__global__ void pf_attn_merge(int T, int pos0, int Hq, int DH, const float *po, const float *pml, float *o) {
+  const int t = blockIdx.x, hq = blockIdx.y, e = threadIdx.x, pos = pos0 + t;
+  if (pos < PA_PIECE || e >= DH) return;
+  const int S = pos / PA_PIECE + 1;
+  const size_t oi = (size_t)t * Hq + hq, stride = (size_t)T * Hq;
+  float M = -INFINITY;
+  for (int zz = 0; zz < S; ++zz) M = fmaxf(M, pml[(zz * stride + oi) * 2]);
+  float num = 0.f, den = 0.f;
+  for (int zz = 0; zz < S; ++zz) {
+    const float w = expf(pml[(zz * stride + oi) * 2] - M);
+    den += w * pml[(zz * stride + oi) * 2 + 1];
+    num += w * po[(zz * stride + oi) * DH + e];
+  }
+  o[oi * DH + e] = num / den;
 }
 
 // argmax over the logits (lowest index on ties), written as the next token to emit.
@@ -456,10 +491,12 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.scale = b.scale;
       a.out = b.q;
       if ((e = tc_project<EPI_QKV>(a, tw + b.tc_off[0], b, st)) != cudaSuccess) return e;
-      // attention over positions 0 .. pos0 + t
-      const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS);
-      if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
-      else pf_attn<2><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o);
+      // attention over positions 0 .. pos0 + t, split into pieces of PA_PIECE positions
+      const int pieces = (pos + T - 1) / PA_PIECE + 1;
+      const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS, pieces);
+      if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o, b.att_o, b.att_ml);
+      else pf_attn<2><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o, b.att_o, b.att_ml);
+      if (pieces > 1) pf_attn_merge<<<dim3(T, p.Hq), p.dh, 0, st>>>(T, pos, p.Hq, p.dh, b.att_o, b.att_ml, b.o);
       // WO + residual
       a.M = d;
       a.K = dq;

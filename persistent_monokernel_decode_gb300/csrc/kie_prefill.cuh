@@ -14,6 +14,7 @@ constexpr int PF_TOKENS = 128;  // prompt tokens per chunk
 // at tc_w + l * tc_layer_stride + tc_off[j] (kie_tcgemm.cuh); tc_b holds one chunk's activation tiles.
 struct PrefillBufs {
   float *x, *h, *q, *o, *a, *scale, *part;
+  float *att_o, *att_ml;  // attention partials: [pieces][PF_TOKENS][Hq][dh] and [pieces][PF_TOKENS][Hq][2]
   const uint8_t *tc_w;
   long long tc_layer_stride, tc_off[4];
   uint8_t *tc_b;
@@ -30,6 +31,10 @@ inline void kie_tc_splits(int Mt, int KT, int n_cta, int *kt_per_split, int *spl
   *kt_per_split = kps;
   *splits = (KT + kps - 1) / kps;
 }
+
+// Attention pieces a prompt position can span: positions per piece, and pieces for max_seq positions.
+constexpr int PF_ATT_PIECE = 512;
+inline int kie_pf_att_pieces(int max_seq) { return (max_seq + PF_ATT_PIECE - 1) / PF_ATT_PIECE; }
 
 // Bytes of the canonical tensor-core tiles of an [M, K] matrix (rows padded to 128, columns to 64).
 inline size_t kie_tc_tile_bytes(int M, int K) { return (size_t)((M + 127) / 128) * ((K + 63) / 64) * 128 * 64 * 2; }

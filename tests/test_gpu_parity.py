@@ -158,6 +158,29 @@ def test_batched_prefill_across_chunks_is_independent_of_the_cut(kie):
     dec.close()
 
 
+def test_prefill_attention_pieces_are_independent_of_the_cut(kie):
+    """A 1,200-token prompt spans three 512-position attention pieces (split and merged) and ten 128-token
+    chunks: whole, in uneven pieces (cuts inside and at piece and chunk boundaries) and teacher-forced decode
+    afterwards must agree bit for bit, the cached K/V rows included, and match the oracle."""
+    cfg = dataclasses.replace(TINY, seed=15)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(15, 1200, cfg.vocab)
+    forced = synth.tokens(16, 4, cfg.vocab)
+    dec = kie.Decoder(cfg, w, max_seq=1216)
+    dec.prefill(prompt)
+    whole = dec.logits()
+    _, whole_steps = dec.decode_forced(forced)
+    dec.reset()
+    for a, b in ((0, 511), (511, 513), (513, 640), (640, 1023), (1023, 1024), (1024, 1200)):
+        dec.prefill(prompt[a:b])
+    np.testing.assert_array_equal(dec.logits(), whole)
+    _, steps = dec.decode_forced(forced)
+    np.testing.assert_array_equal(steps, whole_steps)
+    ref_tokens, ref_logits = oracle.generate(cfg, w, prompt, 0, max_seq=1216)
+    assert float(np.max(np.abs(whole - ref_logits[0]))) <= LOGIT_TOL
+    dec.close()
+
+
 def test_api_errors(tiny, kie):
     _, dec = tiny
     dec.reset()
