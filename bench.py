@@ -83,7 +83,11 @@ def phase_breakdown(dec, model, prompt_len, new):
         release.append((leave[k].min() - arrive[k].max()) / 1e3)
     c_mid = prompt_len + 1 + toks // 2
     b = phase_bytes(model, c_mid)
-    out = {"tokens": f"{toks} tokens from c = {prompt_len + 1}", "release_latency_us": float(np.median(release)),
+    stamps = np.unique(arrive)
+    step = float(np.min(np.diff(stamps))) if stamps.size > 1 else 0.0
+    out = {"tokens": f"{toks} tokens from c = {prompt_len + 1}", "timer_step_ns": step,
+           "note": "%globaltimer stamps advance in timer_step_ns steps: each phase median is quantised to it",
+           "release_latency_us": float(np.median(release)),
            "barrier_us_per_token": float(np.median(release)) * per_tok}
     for n, v in per.items():
         us = float(np.median(v))
