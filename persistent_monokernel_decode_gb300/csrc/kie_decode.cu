@@ -462,9 +462,19 @@ __device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard
       if (moe) {
         // the routed experts are known only once the router has run: wait for the consumers' selection
         ok = ok && wait_mbar(sel.bar, nsel++ & 1u, g);
-        for (int j = 0; j < p.top_k && ok; ++j)
-          ok = produce_region(lw + p.off_egu + (size_t)sel.ids[j] * p.egu_bytes + (size_t)rg.r0 * p.d, rg.r1 - rg.r0,
-                              p.d, s, p.nslot, rp, policy, g, 1, FP8_TILE_COLS);
+        // gate/up: two experts' rows stacked into one tile when each gives at most half a tile of rows
+        const int Re = rg.r1 - rg.r0;
+        const uint8_t *gub = lw + p.off_egu + (size_t)rg.r0 * p.d;
+        if (Re > 0 && 2 * Re <= TILE_ROWS) {
+          for (int j = 0; j < p.top_k && ok; j += 2)
+            ok = produce_stacked_fp8(gub + (size_t)sel.ids[j] * p.egu_bytes,
+                                     j + 1 < p.top_k ? gub + (size_t)sel.ids[j + 1] * p.egu_bytes : nullptr, Re, p.d, s,
+                                     p.nslot, rp, policy, g);
+        } else {
+          for (int j = 0; j < p.top_k && ok; ++j)
+            ok = produce_region(gub + (size_t)sel.ids[j] * p.egu_bytes, Re, p.d, s, p.nslot, rp, policy, g, 1,
+                                FP8_TILE_COLS);
+        }
         for (int j = 0; j < p.top_k && ok; ++j)
           ok = produce_region(lw + p.off_edn + (size_t)sel.ids[j] * p.edn_bytes + (size_t)ro.r0 * p.F, ro.r1 - ro.r0,
                               p.F, s, p.nslot, rp, policy, g, 1, FP8_TILE_COLS);
@@ -582,7 +592,10 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
             cp_async4(scd + i, esd + (size_t)sel.ids[i / Rd] * p.d + ro.r0 + i % Rd);
         }
         // [EXPERT GATE/UP] a_j = silu(gate_j) * up_j for each routed expert j, rows interleaved
-        for (int j = 0; j < p.top_k; ++j) consume_region_fp8(s, p.nslot, rp, Re, p.d, s.vec, inv, s.out + j * Re, g);
+        // two experts per tile when stacked (see the producer): their rows land side by side in s.out
+        const int step = (Re > 0 && 2 * Re <= TILE_ROWS) ? 2 : 1;
+        for (int j = 0; j < p.top_k; j += step)
+          consume_region_fp8(s, p.nslot, rp, min(step, p.top_k - j) * Re, p.d, s.vec, inv, s.out + j * Re, g);
         cp_async_wait_all();
         consumer_sync();
         for (int i = tid; i < p.top_k * (Re / 2); i += NCT) {

@@ -248,6 +248,24 @@ __device__ inline bool produce_region(const uint8_t *region, int R, int K, Smem 
   return true;
 }
 
+// Producer: the same R rows of two FP8 regions (two experts) as ONE region of 2R rows (2R <= TILE_ROWS): for
+// each column block, A's R-row tile then B's, back to back in one slot, i.e. the [2R][w] tile that
+// consume_region_fp8 reads for a 2R-row region. B null: A alone (R rows).
+__device__ inline bool produce_stacked_fp8(const uint8_t *A, const uint8_t *B, int R, int K, Smem &s, int nslot,
+                                           RingPos &rp, uint64_t policy, const Guard &g) {
+  for (int k0 = 0; k0 < K; k0 += FP8_TILE_COLS) {
+    const uint32_t bytes = (uint32_t)R * (uint32_t)min(FP8_TILE_COLS, K - k0);
+    if (!wait_mbar(&s.empty[rp.slot], rp.phase ^ 1u, g)) return false;
+    uint8_t *dst = s.ring + (size_t)rp.slot * SLOT_BYTES;
+    mbar_arrive_expect_tx(&s.full[rp.slot], B ? 2 * bytes : bytes);
+    bulk_g2s(dst, A + (size_t)R * k0, bytes, &s.full[rp.slot], policy);
+    if (B) bulk_g2s(dst + bytes, B + (size_t)R * k0, bytes, &s.full[rp.slot], policy);
+    ++rp.issued;
+    ring_advance(rp, nslot);
+  }
+  return true;
+}
+
 // Producer, before the CTA may exit: wait until every bulk copy it issued has landed (bounded), so no copy
 // writes into the shared memory of a finished CTA.
 __device__ inline void drain_ring(Smem &s, int nslot, const RingPos &rp, const Guard &g) {
