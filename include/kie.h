@@ -58,7 +58,7 @@ typedef struct kie_ctx kie_ctx;
 
 /* Device buffer sizes a ctx needs (bytes), for callers that allocate device memory themselves. */
 typedef struct {
-  size_t weights_bytes;   /* repacked weights + embedding table */
+  size_t weights_bytes;   /* repacked weights + embedding table (+ the prefill's tensor-core tiles, dense models) */
   size_t kv_bytes;        /* K/V cache [n_layers][2][n_kv_heads][max_seq][head_dim] fp16 */
   size_t workspace_bytes; /* activations, split-attention partials, RoPE table, logits, control words */
   int n_cta;              /* CTAs of the persistent grid the layout was planned for */
@@ -85,9 +85,11 @@ int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *s
 
 /* Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 and keep the
  * logits of the last one (so the next decode can start). The tokens go through each layer together, in chunks
- * of up to 128 (batched GEMMs over the packed weights, causal attention over the cache): the same arithmetic
- * as a decode step, and the result does not depend on how a prompt is split over calls. Synchronous.
- * Errors: INVALID (n < 1, bad id), CAPACITY, CUDA. */
+ * of up to 128: the projections are tensor-core GEMMs (tcgen05) over a second copy of the dense weights in the
+ * tensor cores' tile layout, with each fp32 activation split into fp16 high and low parts (fp32-class results);
+ * the causal attention over the cache runs on CUDA cores in 512-position pieces. The result does not depend on
+ * how a prompt is split over calls (bit for bit). Synchronous. Errors: INVALID (n < 1, bad id), CAPACITY, CUDA,
+ * TIMEOUT (a bounded device wait of the GEMM ran out; the sequence is reset). */
 int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n);
 
 /* Greedy decode of n tokens in ONE launch (the hot path). Token i is the argmax of the current logits
