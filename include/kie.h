@@ -87,7 +87,7 @@ int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *s
  * logits of the last one (so the next decode can start). The tokens go through each layer together, in chunks
  * of up to 128: the projections are tensor-core GEMMs (tcgen05) over a second copy of the dense weights in the
  * tensor cores' tile layout, with each fp32 activation split into fp16 high and low parts (fp32-class results);
- * the causal attention over the cache runs on CUDA cores in 512-position pieces. The result does not depend on
+ * the causal attention over the cache runs on the tensor cores too, in 512-position pieces. The result does not depend on
  * how a prompt is split over calls (bit for bit). Synchronous. Errors: INVALID (n < 1, bad id), CAPACITY, CUDA,
  * TIMEOUT (a bounded device wait of the GEMM ran out; the sequence is reset). */
 int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n);

@@ -21,7 +21,7 @@ _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_ROOT, "_build")
 LIB_PATH = os.path.join(_HERE, "libkie.so")
 SOURCES = ("kie_api.cu", "kie_decode.cu", "kie_gemv.cu", "kie_prefill.cu")
-HEADERS = ("kie_layout.h", "kie_device.cuh", "kie_decode.cuh", "kie_prefill.cuh", "kie_tcgemm.cuh")
+HEADERS = ("kie_layout.h", "kie_device.cuh", "kie_decode.cuh", "kie_prefill.cuh", "kie_tcgemm.cuh", "kie_tcattn.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 KIE_OK, KIE_ERR_INVALID, KIE_ERR_OOM, KIE_ERR_CAPACITY = 0, -1, -2, -3

@@ -6,13 +6,14 @@
 //
 // Kernels, per chunk of T tokens:
 //   pf_embed  X[t] = fp32(E[tok[t]])
-//   per layer: pf_rms(X) -> projection QKV (RoPE, K/V append, q) -> pf_attn (causal, over the cache) ->
+//   per layer: pf_rms(X) -> projection QKV (RoPE, K/V append, q) -> ta_attn (causal, over the cache) ->
 //              projection WO (H = X + Wo o) -> pf_rms(H) -> projection GU (A = silu(g) u) -> projection DOWN
 //              (X = H + Wd a)
 //   after the last chunk: pf_rms(last X) -> pf_gemm LM head (one token, CUDA cores) -> pf_argmax (next token)
 // A projection is a tensor-core GEMM (kie_tcgemm.cuh: the chunk's activations split into fp16 high and low
 // parts, tcgen05.mma into TMEM, K split over blocks so that every SM has one) followed by pf_reduce, which adds
-// the K splits in order and applies the epilogue. No sum's order depends on how the prompt is cut into chunks
+// the K splits in order and applies the epilogue. The attention is a tensor-core kernel too (kie_tcattn.cuh:
+// one block per query head and 512-position piece; pf_attn_merge combines the pieces of long contexts). No sum's order depends on how the prompt is cut into chunks
 // (a token's column of the MMA is computed like any other), so a prompt prefilled in pieces leaves bit-identical
 // logits and cache.
 #include <cuda_fp16.h>
@@ -21,13 +22,13 @@
 #include "kie_decode.cuh"
 #include "kie_layout.h"
 #include "kie_prefill.cuh"
+#include "kie_tcattn.cuh"
 #include "kie_tcgemm.cuh"
 
 namespace kie {
 namespace {
 
 constexpr int PF_THREADS = 256;
-constexpr int PA_WARPS = 4;  // tokens (one warp each) per attention block
 constexpr int PA_PIECE = PF_ATT_PIECE;  // positions per attention piece (fixed boundaries 0, 512, 1024, ...)
 constexpr int GR = TILE_ROWS;    // output rows per block pass (a row group of the packed layout)
 constexpr int KC = 32;           // columns per shared-memory stage
@@ -224,167 +225,6 @@ __global__ void pf_embed(const int *tok, int T, const __half *E, int d, float *x
   for (int i = threadIdx.x; i < d; i += blockDim.x) x[(size_t)t * d + i] = __half2float(row[i]);
 }
 
-// Causal attention of T new tokens (positions pos0 .. pos0+T-1) over the cache of one layer. Block: one KV head,
-// PA_WARPS consecutive tokens (a warp per token with all G query heads of the group) and one piece z of the
-// cached positions, [z * PA_PIECE, (z + 1) * PA_PIECE); the 32-position K/V tiles are shared by the block.
-// Scores, online softmax and P.V follow the decode kernel's formulas. A token whose positions fit in one piece
-// writes its output; otherwise every piece writes its partial (m, l, unnormalised o) and pf_attn_merge combines
-// them. Piece boundaries are absolute positions, so a token's arithmetic does not depend on its chunk.
-template <int DPL>
-__global__ void __launch_bounds__(PA_WARPS * 32) pf_attn(const float *q, int T, int pos0, const __half *kvl, int Hq,
-                                                         int Hkv, int max_seq, float *o, float *po, float *pml) {
-  constexpr int DH = DPL * 32, U = DH / 8;
-  __shared__ __align__(16) __half Ks[32 * DH];
-  __shared__ __align__(16) __half Vs[32 * DH];
-  __shared__ __align__(16) float qs[PA_WARPS][MAX_GROUP][DH];
-  __shared__ float ps[PA_WARPS][MAX_GROUP][32];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int kh = blockIdx.x, G = Hq / Hkv;
-  const int t = blockIdx.y * PA_WARPS + warp;
-  const bool live = t < T;
-  const int pos = pos0 + t;  // this warp's query position
-  const int z = blockIdx.z, jlo = z * PA_PIECE;
-  const int last = min(pos0 + min(T, (int)blockIdx.y * PA_WARPS + PA_WARPS) - 1, jlo + PA_PIECE - 1);  // block's end
-  if (jlo > last) return;  // no position of this piece is attended by the block's tokens
-  const size_t plane = (size_t)max_seq * DH;
-  const __half *Kb = kvl + (size_t)kh * plane, *Vb = kvl + (size_t)(Hkv + kh) * plane;
-  const float qscale = 1.0f / sqrtf((float)DH);
-  if (live)
-    for (int i = lane; i < G * DH; i += 32) qs[warp][i / DH][i % DH] = q[(size_t)t * Hq * DH + (size_t)kh * G * DH + i] * qscale;
-  float m[MAX_GROUP], l[MAX_GROUP], acc[MAX_GROUP][DPL];
-#pragma unroll
-  for (int h = 0; h < MAX_GROUP; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) acc[h][e] = 0.f;
-  }
-  constexpr int UPT = 32 * U / (PA_WARPS * 32);  // 16-byte units of a K (or V) tile per thread
-  static_assert(32 * U % (PA_WARPS * 32) == 0, "tile units split evenly over the block");
-  uint4 kreg[UPT], vreg[UPT];
-  auto fetch = [&](int jb) {  // registers <- K, V rows [jb, jb + 32) that exist (zeros past `last`)
-#pragma unroll
-    for (int k = 0; k < UPT; ++k) {
-      const int u = tid + k * PA_WARPS * 32, row = u / U, c = u % U, j = jb + row;
-      kreg[k] = make_uint4(0u, 0u, 0u, 0u);
-      vreg[k] = kreg[k];
-      if (j <= last) {
-        kreg[k] = *reinterpret_cast<const uint4 *>(Kb + (size_t)j * DH + c * 8);
-        vreg[k] = *reinterpret_cast<const uint4 *>(Vb + (size_t)j * DH + c * 8);
-      }
-    }
-  };
-  fetch(jlo);
-  for (int jb = jlo; jb <= last; jb += 32) {
-    __syncthreads();  // the previous tile is no longer read
-#pragma unroll
-    for (int k = 0; k < UPT; ++k) {
-      const int u = tid + k * PA_WARPS * 32, row = u / U, c = u % U;
-      *reinterpret_cast<uint4 *>(Ks + (size_t)row * DH + (size_t)(c ^ (row % U)) * 8) = kreg[k];
-      *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = vreg[k];
-    }
-    __syncthreads();
-    if (jb + 32 <= last) fetch(jb + 32);  // the next tile is in flight while this one is used
-    if (!live || jb > pos) continue;
-    const int j = jb + lane;
-    const bool valid = j <= pos;
-    const __half *kr = Ks + (size_t)lane * DH;
-    float s[MAX_GROUP];
-#pragma unroll
-    for (int h = 0; h < MAX_GROUP; ++h) s[h] = 0.f;
-    for (int c = 0; c < U; ++c) {
-      const uint4 raw = *reinterpret_cast<const uint4 *>(kr + (c ^ (lane % U)) * 8);
-      const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-      const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-      const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.z));
-      const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.w));
-#pragma unroll
-      for (int h = 0; h < MAX_GROUP; ++h) {
-        if (h < G) {
-          const float4 qa = *reinterpret_cast<const float4 *>(&qs[warp][h][8 * c]);
-          const float4 qb = *reinterpret_cast<const float4 *>(&qs[warp][h][8 * c + 4]);
-          float v = s[h];
-          v = fmaf(k0.x, qa.x, v);
-          v = fmaf(k0.y, qa.y, v);
-          v = fmaf(k1.x, qa.z, v);
-          v = fmaf(k1.y, qa.w, v);
-          v = fmaf(k2.x, qb.x, v);
-          v = fmaf(k2.y, qb.y, v);
-          v = fmaf(k3.x, qb.z, v);
-          v = fmaf(k3.y, qb.w, v);
-          s[h] = v;
-        }
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < MAX_GROUP; ++h) {
-      if (h < G) {
-        const float sc = valid ? s[h] : -INFINITY;
-        float mx = sc;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float mnew = fmaxf(m[h], mx);
-        const float e = valid ? expf(sc - mnew) : 0.f;
-        ps[warp][h][lane] = e;
-        float sum = e;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        const float corr = expf(m[h] - mnew);
-        l[h] = l[h] * corr + sum;
-        m[h] = mnew;
-#pragma unroll
-        for (int e2 = 0; e2 < DPL; ++e2) acc[h][e2] *= corr;
-      }
-    }
-    __syncwarp();
-    // P.V: lane owns dims lane*DPL .. +DPL
-    for (int jj = 0; jj < 32; ++jj) {
-      float v[DPL];
-      if (DPL == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(Vs + (size_t)jj * DH + lane * 4);
-        const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 a1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        v[0] = a0.x;
-        v[1] = a0.y;
-        v[2 % DPL] = a1.x;
-        v[3 % DPL] = a1.y;
-      } else {
-        const float2 a0 = __half22float2(*reinterpret_cast<const __half2 *>(Vs + (size_t)jj * DH + lane * 2));
-        v[0] = a0.x;
-        v[1 % DPL] = a0.y;
-      }
-#pragma unroll
-      for (int h = 0; h < MAX_GROUP; ++h)
-        if (h < G) {
-          const float pj = ps[warp][h][jj];
-#pragma unroll
-          for (int e2 = 0; e2 < DPL; ++e2) acc[h][e2] = fmaf(pj, v[e2], acc[h][e2]);
-        }
-    }
-    __syncwarp();
-  }
-  if (!live || jlo > pos) return;
-  const bool single = pos < PA_PIECE;  // the token's only piece
-#pragma unroll
-  for (int h = 0; h < MAX_GROUP; ++h)
-    if (h < G) {
-      const size_t oi = (size_t)t * Hq + (size_t)(kh * G + h);
-      if (single) {
-        const float inv = 1.0f / l[h];
-#pragma unroll
-        for (int e2 = 0; e2 < DPL; ++e2) o[oi * DH + lane * DPL + e2] = acc[h][e2] * inv;
-      } else {
-        const size_t pi = (size_t)z * T * Hq + oi;
-#pragma unroll
-        for (int e2 = 0; e2 < DPL; ++e2) po[pi * DH + lane * DPL + e2] = acc[h][e2];
-        if (lane == 0) {
-          pml[pi * 2] = m[h];
-          pml[pi * 2 + 1] = l[h];
-        }
-      }
-    }
-}
-
 // o of the tokens whose positions span several pieces: pieces in ascending order, w_z = exp(m_z - M),
 // o = sum_z w_z o_z / sum_z w_z l_z. Block: one token and one query head, a thread per dimension.
 __global__ void pf_attn_merge(int T, int pos0, int Hq, int DH, const float *po, const float *pml, float *o) {
@@ -463,6 +303,10 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
   const int d = p.d, dq = p.Hq * p.dh, F = p.F, qkv = (p.Hq + 2 * p.Hkv) * p.dh;
   const size_t plane = (size_t)p.max_seq * p.dh;
   cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TC_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ta_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ta_smem_bytes<128>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(ta_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ta_smem_bytes<64>());
   if (e != cudaSuccess) return e;
   int last_t = 0;
   for (int c0 = 0; c0 < n; c0 += PF_TOKENS) {
@@ -491,11 +335,13 @@ cudaError_t kie_run_prefill(const kie::DecodeParams &p, const kie::PrefillBufs &
       a.scale = b.scale;
       a.out = b.q;
       if ((e = tc_project<EPI_QKV>(a, tw + b.tc_off[0], b, st)) != cudaSuccess) return e;
-      // attention over positions 0 .. pos0 + t, split into pieces of PA_PIECE positions
+      // attention over positions 0 .. pos0 + t on the tensor cores, split into pieces of PA_PIECE positions
       const int pieces = (pos + T - 1) / PA_PIECE + 1;
-      const dim3 ag(p.Hkv, (T + PA_WARPS - 1) / PA_WARPS, pieces);
-      if (p.dh == 128) pf_attn<4><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o, b.att_o, b.att_ml);
-      else pf_attn<2><<<ag, PA_WARPS * 32, 0, st>>>(b.q, T, pos, kvl, p.Hq, p.Hkv, p.max_seq, b.o, b.att_o, b.att_ml);
+      const TaArgs ta{b.q, kvl, b.o, b.att_o, b.att_ml, T, pos, p.Hq, p.Hkv, p.max_seq, b.status, b.timeout_ns};
+      if (p.dh == 128)
+        ta_attn_kernel<128><<<dim3(p.Hq, pieces), TA_THREADS, ta_smem_bytes<128>(), st>>>(ta);
+      else
+        ta_attn_kernel<64><<<dim3(p.Hq, pieces), TA_THREADS, ta_smem_bytes<64>(), st>>>(ta);
       if (pieces > 1) pf_attn_merge<<<dim3(T, p.Hq), p.dh, 0, st>>>(T, pos, p.Hq, p.dh, b.att_o, b.att_ml, b.o);
       // WO + residual
       a.M = d;
