@@ -42,6 +42,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16-byte asynchronous global -> shared copy; bytes past src_bytes (0 or 16) are zero-filled.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
 template <int DH>
 constexpr size_t ta_smem_bytes() {
   return (size_t)2 * TA_M * DH * 2    // Q hi, lo
@@ -109,22 +115,30 @@ __global__ void __launch_bounds__(TA_THREADS, 1) ta_attn_kernel(const TaArgs a) 
   uint32_t nmma = 0;  // completions of mbar so far
   bool ok = true;
 
-  // stage K (and, if with_v, V transposed) for positions [kt, kt + TA_N) (zero past jhi)
+  // stage K (and, if with_v, V transposed) for positions [kt, kt + TA_N) (zero past jhi). K moves by
+  // asynchronous copies; the thread's V loads are all issued before the transposing stores, so every load of
+  // the tile is in flight at once.
+  constexpr int PER = TA_N * (DH / 8) / TA_THREADS;  // 16-byte pieces per thread per tile
+  static_assert(TA_N * (DH / 8) % TA_THREADS == 0, "tile pieces split evenly over the block");
   auto stage = [&](int kt, bool with_v) {
-    for (int i = tid; i < TA_N * (DH / 8); i += TA_THREADS) {
-      const int p = i / (DH / 8), k0 = (i % (DH / 8)) * 8, j = kt + p;
-      uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-      if (j < jhi) {
-        kv = *reinterpret_cast<const uint4 *>(Kb + (size_t)j * DH + k0);
-        if (with_v) vv = *reinterpret_cast<const uint4 *>(Vb + (size_t)j * DH + k0);
-      }
-      *reinterpret_cast<uint4 *>(sK + ta_offset(p, k0, DH)) = kv;
-      if (with_v) {
-        const __half *vh = reinterpret_cast<const __half *>(&vv);
+    uint4 vv[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int i = tid + u * TA_THREADS, p = i / (DH / 8), k0 = (i % (DH / 8)) * 8, j = kt + p;
+      const bool in = j < jhi;
+      cp_async16(sK + ta_offset(p, k0, DH), Kb + (in ? (size_t)j * DH + k0 : 0), in ? 16u : 0u);
+      if (with_v) vv[u] = in ? *reinterpret_cast<const uint4 *>(Vb + (size_t)j * DH + k0) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (with_v) {
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int i = tid + u * TA_THREADS, p = i / (DH / 8), k0 = (i % (DH / 8)) * 8;
+        const __half *vh = reinterpret_cast<const __half *>(&vv[u]);
 #pragma unroll
         for (int e = 0; e < 8; ++e) *reinterpret_cast<__half *>(sV + ta_offset(k0 + e, p, TA_N)) = vh[e];
       }
     }
+    cp_async_wait_all();
     fence_proxy_async_smem();
     __syncthreads();
   };
