@@ -233,6 +233,12 @@ int kie_create_moe_with_buffers(const kie_config *cfg, const kie_moe_config *moe
  * (column blocks of 512 codes). M even, K a multiple of 16; -1 for bad arguments. */
 int64_t kie_packed_offset_fp8(int M, int K, int n_cta, int r, int c);
 
+/* Host-side layout query (no GPU needed): byte offset of W[r][c] inside the prefill's tensor-core copy of an
+ * [M, K] fp16 matrix: 128-row x 64-column tiles of 16 KB (rows padded to 128, columns to 64), tile (i, j) at
+ * (i * ceil(K / 64) + j) * 16 KB, inside a tile 8 x 8 core matrices of 128 contiguous bytes (the canonical
+ * K-major layout the tensor-core instructions read without swizzle). -1 for bad arguments. */
+int64_t kie_tc_tile_offset(int M, int K, int r, int c);
+
 /* Host-side layout query (no GPU needed): element offset of W[r][c] inside the packed matrix. */
 int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c);
 

@@ -153,6 +153,7 @@ SIGNATURES = {
     "kie_create_moe_with_buffers": ([P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t, P, ctypes.c_size_t, P],
                                     ctypes.c_int),
     "kie_packed_offset_fp8": ([ctypes.c_int] * 5, ctypes.c_int64),
+    "kie_tc_tile_offset": ([ctypes.c_int] * 4, ctypes.c_int64),
 }
 
 _lib = None
@@ -384,6 +385,10 @@ def gemv(packed, x, M: int, K: int, n_cta: int = 0, y=None):
 
 def packed_offset(M: int, K: int, n_cta: int, r: int, c: int) -> int:
     return lib().kie_packed_offset(M, K, n_cta, r, c)
+
+
+def tc_tile_offset(M: int, K: int, r: int, c: int) -> int:
+    return lib().kie_tc_tile_offset(M, K, r, c)
 
 
 def packed_offset_fp8(M: int, K: int, n_cta: int, r: int, c: int) -> int:

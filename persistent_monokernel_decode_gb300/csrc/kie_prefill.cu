@@ -19,6 +19,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "kie.h"
 #include "kie_decode.cuh"
 #include "kie_layout.h"
 #include "kie_prefill.cuh"
@@ -391,4 +392,11 @@ cudaError_t kie_launch_tc_pack(const uint16_t *src, int M, int K, const uint16_t
   const long long n = (long long)Mp * KT * (kie::TC_KT / 8);
   kie::tc_pack_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(src, M, K, KT, gain, dst);
   return cudaGetLastError();
+}
+
+// Host-side layout query of include/kie.h: byte offset of W[r][c] in the tensor-core copy of an [M, K] matrix.
+extern "C" int64_t kie_tc_tile_offset(int M, int K, int r, int c) {
+  if (M < 1 || K < 8 || K % 8 || r < 0 || r >= M || c < 0 || c >= K) return -1;
+  const int KT = (K + 63) / 64;
+  return ((int64_t)(r / 128) * KT + c / 64) * (128 * 64 * 2) + kie::kie_tc_offset_in_tile(r % 128, c % 64);
 }

@@ -36,6 +36,10 @@ inline void kie_tc_splits(int Mt, int KT, int n_cta, int *kt_per_split, int *spl
 constexpr int PF_ATT_PIECE = 512;
 inline int kie_pf_att_pieces(int max_seq) { return (max_seq + PF_ATT_PIECE - 1) / PF_ATT_PIECE; }
 
+// Byte offset of element (r, k) in a canonical 128 x 64 tensor-core tile (8 x 8 fp16 core matrices of 128
+// contiguous bytes; core matrix (i, j) at i * 1024 + j * 128). The device code's tc_tile_offset is the same map.
+inline int kie_tc_offset_in_tile(int r, int k) { return (r >> 3) * 1024 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2; }
+
 // Bytes of the canonical tensor-core tiles of an [M, K] matrix (rows padded to 128, columns to 64).
 inline size_t kie_tc_tile_bytes(int M, int K) { return (size_t)((M + 127) / 128) * ((K + 63) / 64) * 128 * 64 * 2; }
 

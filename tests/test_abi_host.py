@@ -76,6 +76,26 @@ def test_fp8_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
     assert kie.packed_offset_fp8(M, K + 8, n, 0, 0) == -1  # K must be a multiple of 16
 
 
+@pytest.mark.parametrize("M,K", [(128, 64), (256, 128), (200, 200), (768, 256), (136, 72)])
+def test_tensor_core_tile_layout_is_canonical(M, K):
+    """The prefill's tensor-core copy: an injective map into ceil(M/128) x ceil(K/64) tiles of 16 KB, each 8-row x
+    8-column block one run of 128 bytes with rows 16 bytes apart (the no-swizzle core matrix), core matrices 128 B
+    apart along K and 1 KB apart along M: the strides the tensor-core descriptors are given."""
+    off = np.array([[kie.tc_tile_offset(M, K, r, c) for c in range(K)] for r in range(M)], dtype=np.int64)
+    KT, MT = (K + 63) // 64, (M + 127) // 128
+    assert off.min() >= 0 and off.max() < MT * KT * 16384 and len(np.unique(off)) == M * K
+    assert np.all(off % 2 == 0)
+    for r in range(0, M - 7, 8):
+        for c in range(0, K - 7, 8):
+            blk = off[r:r + 8, c:c + 8]
+            assert np.array_equal(blk - blk[0, 0], np.arange(8)[:, None] * 16 + np.arange(8)[None, :] * 2)
+            if (c + 8) % 64 and c + 15 < K:
+                assert off[r, c + 8] - off[r, c] == 128          # next core matrix along K
+            if (r + 8) % 128 and r + 15 < M:
+                assert off[r + 8, c] - off[r, c] == 1024         # next 8-row group
+    assert kie.tc_tile_offset(M, K + 4, 0, 0) == -1             # K must be a multiple of 8
+
+
 def test_moe_buffer_plan_without_a_device():
     cfg = kie.make_config(MOE_M, 768)
     s = kie.kie_query_buffers(cfg, 152, kie.make_moe_config(MOE_M))
