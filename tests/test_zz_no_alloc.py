@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import synth
-from synth.configs import TINY, TINY_DECODE, ModelConfig
+from synth.configs import MOE_TINY, TINY, TINY_DECODE, ModelConfig
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,7 @@ def kie():
 
 def two_calls_each_way(kie, cfg, prompt, n1, n2, max_seq):
     import torch
-    w = synth.model_weights(cfg)
+    w = synth.moe_weights(cfg) if getattr(cfg, "n_experts", 0) else synth.model_weights(cfg)
     dec = kie.Decoder(cfg, w, max_seq=max_seq)
     try:
         dec.prefill(prompt)
@@ -61,6 +61,12 @@ def test_noalloc_matches_decode_gqa_dh128(kie):
     cfg = ModelConfig("na", n_layers=2, d_model=384, n_heads=8, n_kv_heads=2, head_dim=128, ffn_dim=1000,
                       vocab=1000, seed=21, gain_std=0.1)
     two_calls_each_way(kie, cfg, synth.tokens(21, 40, cfg.vocab), 7, 7, 64)
+
+
+def test_noalloc_matches_decode_sparse_moe(kie):
+    """The sparse-MoE kernel (router logits and the routed experts' selection in the scratch) through the
+    no-allocation entry point."""
+    two_calls_each_way(kie, MOE_TINY, synth.tokens(MOE_TINY.seed, 10, MOE_TINY.vocab), 6, 5, 32)
 
 
 def test_noalloc_and_regular_calls_interleave(kie):
