@@ -6,9 +6,10 @@
 // bulk copies, and four warps read the accumulator back with tcgen05.ld.
 //
 // Precision: the activations are fp32. Each input x is split into two fp16 values, hi = fp16(x) and
-// lo = fp16(x - hi), so that hi + lo carries about 22 significant bits; the tensor core forms W'·hi and W'·lo
-// (fp16 products are exact in fp32) and accumulates in fp32, and the epilogue adds the two. The B operand of
-// one MMA is therefore 256 columns: the chunk's 128 tokens' high parts, then their low parts.
+// lo = fp16(x - hi): hi + lo is within 2^-21 |x| of x while lo is a normal fp16 (|x| >= 2^-3) and within 2^-25
+// absolute below; the tensor core forms W'·hi and W'·lo (fp16 products are exact in fp32) and accumulates in
+// fp32, and the epilogue adds the two, so a projection stays within about 1e-5 of sum |W' x| of the exact one.
+// The B operand of one MMA is therefore 256 columns: the chunk's 128 tokens' high parts, then their low parts.
 //
 // Operand layout (both K-major, no swizzle): a tile is made of 8 x 8 fp16 "core matrices" of 128 contiguous
 // bytes; core matrix (i, j) of rows 8i..8i+7 and columns 8j..8j+7 of a 64-column tile sits at i * 1024 + j * 128.
