@@ -137,6 +137,25 @@ def test_prefill_in_pieces_equals_whole(tiny):
     np.testing.assert_array_equal(dec.logits(), a)
 
 
+def test_prefill_equals_teacher_forced_decode_of_the_prompt(tiny):
+    """prefill(P) then the next token's logits equal those of prefill(P[0]) followed by a teacher-forced decode of
+    P[1:] (the batched tensor-core prefill against the decode kernel, token by token): within twice the logit
+    tolerance of each other (each is within the tolerance of the oracle), and the same greedy token."""
+    _, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    batched = dec.logits()
+    dec.reset()
+    dec.prefill(prompt[:1])
+    dec.decode_forced(prompt[1:], want_logits=False)
+    stepped = dec.logits()
+    assert dec.position == len(prompt)
+    assert float(np.max(np.abs(batched - stepped))) <= 2 * LOGIT_TOL
+    if margins(batched) > 2 * MARGIN:
+        assert int(np.argmax(batched)) == int(np.argmax(stepped))
+
+
 def test_batched_prefill_across_chunks_is_independent_of_the_cut(kie):
     """A 300-token prompt spans three 128-token prefill chunks; prefilled whole or in uneven pieces it must
     leave bit-identical logits (every sum runs in an order the chunking does not change), and both must match
