@@ -174,6 +174,13 @@ def profiled_traffic(workload, digest):
     return float(t.group(1))
 
 
+def roofline(bytes_per_step, step_s, peak_gbs):
+    """Achieved GB/s of a step that must move bytes_per_step in step_s seconds, and its fraction of peak_gbs
+    (MBU when the bytes are the weight and K/V bytes the tokens read)."""
+    achieved = bytes_per_step / step_s / 1e9
+    return achieved, achieved / peak_gbs
+
+
 def algorithmic_bytes(model, prompt_len, n):
     """Bytes one decode of n tokens must move: every weight once per token, plus the K/V prefix it attends
     over (the token at position p attends over p + 1 positions)."""
@@ -480,7 +487,7 @@ def main():
 
     peaks, peak_kind = measured_peaks()
     bytes_launch = algorithmic_bytes(model, prompt_len, new)
-    achieved = bytes_launch / step_s / 1e9
+    achieved, frac = roofline(bytes_launch, step_s, peaks["hbm_gbs"])
     line = {
         "metric": MOE_METRIC if args.moe else METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
@@ -496,7 +503,7 @@ def main():
                 "timed": f"reset + prefill({prompt_len}-token host prompt) + decode({new} -> host array), wall clock"},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(workload, kie.source_digest()),
+                     "frac": frac, "traffic": profiled_traffic(workload, kie.source_digest()),
                      "peak_kind": f"{peak_kind} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": bytes_launch},
         "mbu": {"measured_peak": achieved / peaks["hbm_gbs"], "spec_8tbs": achieved / 8000.0},

@@ -47,3 +47,32 @@ def test_traffic_is_reported_only_for_matching_sources():
     assert t is None or 0.99 < t / bench.algorithmic_bytes(TWO_B, 128, 1024) < 1.01
     assert bench.profiled_traffic("llama2b_p128_n1024", "0" * 16) is None
     assert bench.profiled_traffic("no_such_workload", digest) is None
+
+
+def _golden(name):
+    vals = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", name)):
+        line = line.split("#", 1)[0].strip()
+        if line:
+            k, v = (x.strip() for x in line.split("="))
+            vals[k] = float(v)
+    return vals
+
+
+def test_roofline_arithmetic_reproduces_the_pages_worked_numbers():
+    """The pages' own example of the bandwidth roofline (8 GPUs' aggregate bandwidth over a 2B model's ~4 GB of
+    fp16 weights gives ~8,400 tok/s, of which ~3,000 tok/s is ~36 %) and of the launch tax (4.5 us x 10 kernels x
+    25 layers per token caps decode near 890 tok/s; 3,000 tok/s leaves ~333 us per token), through the same
+    roofline function the bench reports with."""
+    g = _golden("roofline_arithmetic.txt")
+    bytes_per_token = g["active_weight_gb"] * 1e9
+    peak_gbs = g["aggregate_bandwidth_tbs"] * 1e3
+    ceiling = peak_gbs * 1e9 / bytes_per_token
+    assert abs(ceiling - g["ceiling_tok_s"]) / g["ceiling_tok_s"] < 0.01
+    # one second of decode at the reported rate: the fraction of the ceiling is the MBU-style fraction
+    _, frac = bench.roofline(bytes_per_token * g["target_tok_s"], 1.0, peak_gbs)
+    assert abs(frac - g["fraction_of_ceiling"]) < 0.005
+    tax = g["launch_us_per_kernel"] * g["kernels_per_layer"] * g["layers"]
+    assert tax == g["launch_tax_us_per_token"]
+    assert abs(1e6 / tax - g["launch_bound_tok_s"]) / g["launch_bound_tok_s"] < 0.01
+    assert abs(1e6 / g["target_tok_s"] - g["budget_us_per_token"]) < 0.5
