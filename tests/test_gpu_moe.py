@@ -140,13 +140,16 @@ def test_moe_joint_expert_permutation_leaves_the_logits_bit_identical(kie):
 
 
 # structure variants: one routed expert (weight exactly 1), every expert routed, several router logits per
-# lane (40 experts), the largest router (256 experts), and widths with full and ragged 512-code FP8 blocks
+# lane (40 experts), the largest router (256 experts), widths with full and ragged 512-code FP8 blocks, and
+# experts wide enough that some CTAs stack two experts' gate/up tiles and others do not
 MOE_VARIANTS = {
     "top1": dict(top_k=1),
     "all_experts": dict(top_k=8),
     "e40_k3": dict(n_experts=40, top_k=3),
     "e256_k8": dict(n_experts=256, top_k=8, n_layers=1),
     "wide_ragged": dict(d_model=784, ffn_dim=528, expert_ffn=528, top_k=2, n_layers=1),
+    # 2,560 gate/up rows over 152 CTAs: 16 rows (two experts stacked per tile) or 18 (one expert per tile)
+    "wide_experts": dict(ffn_dim=1280, expert_ffn=1280, top_k=3, n_layers=1),
 }
 
 
