@@ -68,6 +68,7 @@ def lib():
             "orc_e4m3_to_double": ([ctypes.c_uint8], d),
             "orc_gemv_fp8_f32": ([P, P, P, i, i, P], None), "orc_gemv_fp8_f64": ([P, P, P, i, i, P], None),
             "orc_topk_softmax_f64": ([P, i, i, P, P], None), "orc_route_margin": ([P, i], d),
+            "orc_route_ids": ([P, P, P], i),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -220,17 +221,30 @@ class Model:
     def reset(self) -> None:
         lib().orc_reset(self._h)
 
-    def forward(self, token: int) -> np.ndarray:
-        logits = np.empty(self.cfg.vocab, dtype=_real(self.precision))
-        if lib().orc_forward(self._h, int(token), logits.ctypes.data) != 0:
+    def forward(self, token: int, want_logits: bool = True):
+        """One forward at the current position; its logits, or None when want_logits is False (the final norm
+        and LM head are then skipped; cache and state are the same)."""
+        logits = np.empty(self.cfg.vocab, dtype=_real(self.precision)) if want_logits else None
+        if lib().orc_forward(self._h, int(token), logits.ctypes.data if want_logits else None) != 0:
             raise ValueError("oracle forward refused (cache full or token out of range)")
         return logits
 
     def prefill(self, tokens) -> np.ndarray:
-        logits = None
-        for t in tokens:
-            logits = self.forward(t)
-        return logits
+        """Forward every prompt token; the logits of the last one (the others' LM heads are skipped)."""
+        tokens = list(tokens)
+        for t in tokens[:-1]:
+            self.forward(t, want_logits=False)
+        return self.forward(tokens[-1]) if tokens else None
+
+    def route(self):
+        """The routing of the last forward (sparse-MoE models): (ids [n_layers, top_k] in selection order,
+        gaps [n_layers]: each layer's k-th selected router logit minus its best unselected one)."""
+        L, k = self.cfg.n_layers, self.cfg.top_k
+        ids = np.empty((L, k), dtype=np.int32)
+        gaps = np.empty(L, dtype=np.float64)
+        if lib().orc_route_ids(self._h, ids.ctypes.data, gaps.ctypes.data) != 0:
+            raise ValueError("not a sparse-MoE model")
+        return ids, gaps
 
     def moe_ffn(self, layer: int, u) -> np.ndarray:
         """The sparse-MoE FFN output of `layer` for a normalised input u."""

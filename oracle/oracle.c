@@ -64,6 +64,8 @@ typedef struct {
   void *x, *u, *q, *k, *v, *o, *t, *g, *up, *scores;
   void *rl, *acc; /* MoE: router logits [E], FFN output [d] */
   double route_margin; /* MoE diagnostic: smallest gap between the last selected and the best unselected logit */
+  int *route_ids;      /* MoE: experts selected by each layer of the last forward [L][top_k], in selection order */
+  double *route_gap;   /* MoE: that layer's gap (k-th selected logit minus the best unselected one) [L] */
 } orc_model;
 
 /* ---- binary16 <-> real, from the format's definition ---------------------------------------------- */
@@ -214,6 +216,9 @@ void orc_attention_f64(const double *q, const uint16_t *K, const uint16_t *V, in
   free(sc);
 }
 
+void orc_destroy(orc_model *m);
+
+/* NULL on a bad cfg or a failed host allocation (nothing is leaked). */
 orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision) {
   half_init();
   if (!cfg || !w || (precision != 32 && precision != 64)) return NULL;
@@ -222,11 +227,16 @@ orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision
       cfg->vocab <= 0 || cfg->max_seq <= 0)
     return NULL;
   orc_model *m = (orc_model *)calloc(1, sizeof(orc_model));
-  if (m) m->route_margin = INFINITY;
+  if (!m) return NULL;
+  m->route_margin = INFINITY;
   m->cfg = *cfg;
   m->precision = precision;
   int L = cfg->n_layers;
   m->ptrs = (const uint16_t **)calloc((size_t)(9 * (L > 0 ? L : 1)), sizeof(uint16_t *));
+  if (!m->ptrs) {
+    orc_destroy(m);
+    return NULL;
+  }
   const uint16_t *const *src[9] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
   const uint16_t *const **dst[9] = {&m->w.attn_norm, &m->w.wq, &m->w.wk, &m->w.wv, &m->w.wo,
                                     &m->w.ffn_norm, &m->w.w_gate, &m->w.w_up, &m->w.w_down};
@@ -251,7 +261,11 @@ orc_model *orc_create(const orc_config *cfg, const orc_weights *w, int precision
   m->t = calloc((size_t)wide, es);
   m->g = calloc((size_t)cfg->ffn_dim, es);
   m->up = calloc((size_t)cfg->ffn_dim, es);
-  m->scores = calloc((size_t)cfg->max_seq, es);
+  m->scores = calloc((size_t)cfg->max_seq * cfg->n_heads, es); /* one score row per query head */
+  if (!m->kv || !m->x || !m->u || !m->q || !m->k || !m->v || !m->o || !m->t || !m->g || !m->up || !m->scores) {
+    orc_destroy(m);
+    return NULL;
+  }
   return m;
 }
 
@@ -261,6 +275,8 @@ void orc_destroy(orc_model *m) {
   free(m->moe_ptrs);
   free(m->rl);
   free(m->acc);
+  free(m->route_ids);
+  free(m->route_gap);
   free(m->kv);
   free(m->x); free(m->u); free(m->q); free(m->k); free(m->v);
   free(m->o); free(m->t); free(m->g); free(m->up); free(m->scores);
@@ -270,7 +286,8 @@ void orc_destroy(orc_model *m) {
 int orc_pos(const orc_model *m) { return m->pos; }
 void orc_reset(orc_model *m) { m->pos = 0; }
 
-/* Forward one token; logits is float[vocab] (precision 32) or double[vocab] (precision 64).
+/* Forward one token; logits is float[vocab] (precision 32) or double[vocab] (precision 64), or NULL to skip the
+ * final norm and LM head (a prompt position whose logits are not needed; the cache and state are the same).
  * Returns 0, or -1 when the cache is full or the token is out of range. */
 int orc_forward(orc_model *m, int token, void *logits) {
   if (m->pos >= m->cfg.max_seq || token < 0 || token >= m->cfg.vocab) return -1;
@@ -324,8 +341,25 @@ int orc_set_moe(orc_model *m, const orc_moe *moe) {
   m->up = calloc((size_t)gmax, es);
   free(m->rl);
   free(m->acc);
+  free(m->route_ids);
+  free(m->route_gap);
   m->rl = calloc((size_t)moe->n_experts, es);
   m->acc = calloc((size_t)d, es);
+  m->route_ids = (int *)calloc((size_t)L * moe->top_k, sizeof(int));
+  m->route_gap = (double *)calloc((size_t)L, sizeof(double));
+  if (!m->moe_ptrs || !m->g || !m->up || !m->rl || !m->acc || !m->route_ids || !m->route_gap) return -1;
+  return 0;
+}
+
+/* The routing of the last forward: ids [n_layers][top_k] (each layer's experts in selection order: descending
+ * router logit, the lowest id first among equal ones) and gaps [n_layers] (that layer's k-th selected logit
+ * minus its best unselected one; +inf when every expert is selected). Either may be NULL. Returns -1 for a dense
+ * model. */
+int orc_route_ids(const orc_model *m, int *ids, double *gaps) {
+  if (!m || m->moe.n_experts < 1) return -1;
+  const int L = m->cfg.n_layers;
+  if (ids) memcpy(ids, m->route_ids, sizeof(int) * (size_t)L * m->moe.top_k);
+  if (gaps) memcpy(gaps, m->route_gap, sizeof(double) * (size_t)L);
   return 0;
 }
 

@@ -119,6 +119,8 @@ static void NAME(moe_ffn)(orc_model *m, int l, const REAL *u, REAL *out) {
     }
     const double gap = (double)rl[idx[mo->top_k - 1]] - best_out;
     if (gap < m->route_margin) m->route_margin = gap;
+    m->route_gap[l] = gap;
+    for (int j = 0; j < mo->top_k; ++j) m->route_ids[(size_t)l * mo->top_k + j] = idx[j];
   }
   for (int i = 0; i < d; ++i) out[i] = 0;
   for (int j = 0; j < mo->top_k; ++j) {
@@ -132,7 +134,8 @@ static void NAME(moe_ffn)(orc_model *m, int l, const REAL *u, REAL *out) {
 }
 
 /* One decoder forward of `token` at position m->pos: appends K and V (rounded to fp16) to the cache,
- * writes the logits of the next position, advances pos. */
+ * writes the logits of the next position (skipped when logits is NULL: a prompt position whose logits are not
+ * wanted), advances pos. */
 static void NAME(forward)(orc_model *m, int token, REAL *logits) {
   const orc_config *c = &m->cfg;
   const int d = c->d_model, Hq = c->n_heads, Hkv = c->n_kv_heads, dh = c->head_dim, F = c->ffn_dim;
@@ -157,9 +160,12 @@ static void NAME(forward)(orc_model *m, int token, REAL *logits) {
         Kl[h * S + (size_t)pos * dh + e] = half_bits((double)k[h * dh + e]);
         Vl[h * S + (size_t)pos * dh + e] = half_bits((double)v[h * dh + e]);
       }
+    /* heads are independent: each gets its own score row, so running them on several threads changes no sum */
+#pragma omp parallel for schedule(static) if (pos >= 255)
     for (int h = 0; h < Hq; ++h) {
       int kvh = h / group;
-      NAME(attention)(q + h * dh, Kl + kvh * S, Vl + kvh * S, pos + 1, dh, (size_t)dh, sc, o + h * dh);
+      NAME(attention)(q + h * dh, Kl + kvh * S, Vl + kvh * S, pos + 1, dh, (size_t)dh, sc + (size_t)h * c->max_seq,
+                      o + h * dh);
     }
     NAME(gemv)(m->w.wo[l], o, d, Hq * dh, t);
     for (int i = 0; i < d; ++i) x[i] += t[i];
@@ -177,7 +183,9 @@ static void NAME(forward)(orc_model *m, int token, REAL *logits) {
     NAME(gemv)(m->w.w_down[l], g, d, F, t);
     for (int i = 0; i < d; ++i) x[i] += t[i];
   }
-  NAME(rmsnorm)(x, m->w.final_norm, d, (REAL)c->rms_eps, u);
-  NAME(gemv)(m->w.lm_head, u, c->vocab, d, logits);
+  if (logits) {
+    NAME(rmsnorm)(x, m->w.final_norm, d, (REAL)c->rms_eps, u);
+    NAME(gemv)(m->w.lm_head, u, c->vocab, d, logits);
+  }
   m->pos = pos + 1;
 }

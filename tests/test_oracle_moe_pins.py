@@ -119,6 +119,8 @@ def test_moe_ffn_uses_the_routed_experts_with_their_softmax_weights():
     # the routing margin: 4th selected logit (0.25) minus the best unselected one (0.0)
     assert m.route_margin() == 0.25 and m.route_margin() == np.inf
     sel = [6, 1, 4, 3]
+    ids, gaps = m.route()  # the routing record of layer 0: the experts in selection order and its gap
+    assert list(ids[0]) == sel and gaps[0] == 0.25
     wts = scipy_special.softmax(col.astype(np.float64)[sel])
     ref = sum(wt * _swiglu_expert(lay, e, u) for wt, e in zip(wts, sel))
     np.testing.assert_allclose(got, ref, rtol=1e-9, atol=1e-12)

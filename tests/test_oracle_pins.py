@@ -309,3 +309,34 @@ def test_oracle_rejects_bad_config_and_full_cache():
     m.forward(2)
     with pytest.raises(ValueError):
         m.forward(3)
+
+
+def test_prompt_positions_without_logits_leave_the_same_state():
+    """Skipping the LM head at prompt positions (prefill) changes nothing the next forward sees."""
+    cfg = small_cfg(n_layers=2)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(3, 9, cfg.vocab)
+    a = oracle.Model(cfg, w, 16)
+    la = a.prefill(prompt)
+    b = oracle.Model(cfg, w, 16)
+    lb = [b.forward(t) for t in prompt][-1]
+    np.testing.assert_array_equal(la, lb)
+    np.testing.assert_array_equal(a.forward(5), b.forward(5))
+    assert a.pos == b.pos == len(prompt) + 1
+
+
+def test_attention_heads_on_several_threads_change_no_sum():
+    """Past 256 positions the heads run on several threads, each with its own score row: the logits must be
+    bit-identical to a single-threaded run."""
+    cfg = small_cfg(n_layers=1, n_heads=8, n_kv_heads=2)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(4, 300, cfg.vocab)
+    before = oracle.threads()
+    try:
+        oracle.set_threads(1)
+        one = oracle.Model(cfg, w, 320).prefill(prompt)
+        oracle.set_threads(4)
+        four = oracle.Model(cfg, w, 320).prefill(prompt)
+    finally:
+        oracle.set_threads(before)
+    np.testing.assert_array_equal(one, four)
