@@ -7,6 +7,11 @@
  * Engine pages ("Inside the monokernel: a single resident GPU program that never returns control"): the
  * host launches once, the device embeds, projects, attends, samples and feeds the next token back itself.
  *
+ * Where the calls come from: the pages define no programming interface (the creeta article, section "Before
+ * adopting", only says the engine can stand in for a vLLM deployment). The create / prefill / decode / destroy
+ * shape below is this library's own statement of the batch-1 decode problem; each declaration names the part
+ * of the pages its work follows, or says that it has none.
+ *
  * Conventions for every entry point:
  *   - Return value: KIE_OK (0) or a negative KIE_ERR_* code. kie_last_error() gives a message.
  *   - Weights are IEEE binary16 bit patterns (uint16_t), row-major [out_features, in_features].
@@ -83,7 +88,9 @@ int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *s
                             size_t weights_bytes, void *kv_dev, size_t kv_bytes, void *workspace_dev,
                             size_t workspace_bytes, kie_ctx **out);
 
-/* Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 and keep the
+/* Prompt ingestion. The pages do not describe prefill (their measurements start at decode); this call exists
+ * so that decode has a KV cache and current logits to start from.
+ * Append n prompt tokens (host int32 ids in [0, vocab)) to the KV cache at positions pos..pos+n-1 and keep the
  * logits of the last one (so the next decode can start). The tokens go through each layer together, in chunks
  * of up to 128: the projections are tensor-core GEMMs (tcgen05) over a second copy of the dense weights in the
  * tensor cores' tile layout, with each fp32 activation split into fp16 high and low parts (fp32-class results);
@@ -92,7 +99,9 @@ int kie_create_with_buffers(const kie_config *cfg, const kie_weights *w, void *s
  * TIMEOUT (a bounded device wait of the GEMM ran out; the sequence is reset). */
 int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n);
 
-/* Greedy decode of n tokens in ONE launch (the hot path). Token i is the argmax of the current logits
+/* The monokernel's token loop ("Inside the monokernel", creeta: one resident launch embeds, runs every layer,
+ * samples greedily on the device and feeds the token back, with no host round trip between tokens).
+ * Greedy decode of n tokens in ONE launch (the hot path). Token i is the argmax of the current logits
  * (lowest id on ties); the kernel then runs the forward of that token at the next position, whose logits
  * are the current ones for token i+1. So n tokens cost n forwards, and decode(a) then decode(b) gives the
  * same tokens as decode(a+b). Requires a prior prefill (INVALID otherwise). `out_tokens` is a host array of
@@ -107,19 +116,37 @@ int kie_decode_async(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
 /* Wait for the ctx stream and report the status word of the last launch (KIE_OK or KIE_ERR_TIMEOUT). */
 int kie_sync(kie_ctx *ctx);
 
-/* Teacher forcing, for tests: for i in [0, n): out_tokens[i] = argmax of the current logits (what greedy
+/* No counterpart on the pages: a testing aid of this library (teacher forcing keeps one permitted divergence
+ * of a near-tied greedy choice from cascading when the GPU is compared with a CPU reference).
+ * Teacher forcing, for tests: for i in [0, n): out_tokens[i] = argmax of the current logits (what greedy
  * decode would emit), then the forward consumes forced[i] (not the argmax) at the next position; if
  * out_logits is not NULL it receives the logits of that forward ([n, vocab] fp32, host). Synchronous.
  * Requires a prior prefill. */
 int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_tokens, float *out_logits);
 
-/* Copy the current logits (those the next emitted token is the argmax of) to host float[vocab]. */
+/* No counterpart on the pages: a testing aid for sparse-MoE models (below). The expert selection is itself a
+ * floating-point decision (a top_k over router logits) that a CPU reference and the GPU take from logits rounded
+ * differently; to compare every step, the reference's own selections can be imposed on the GPU.
+ * As kie_decode_forced, plus: forced_experts (host int32 [n][n_layers][top_k], or NULL) replaces the selection
+ * of every layer of every forward by the given expert ids (the routing weights stay the softmax of the GPU's
+ * router logits over the given experts, in the given order); out_experts (host int32 [n][n_layers][top_k], or
+ * NULL) receives the GPU's own selection (descending router logit, the lowest id first among equal ones),
+ * computed whether or not it is overridden. It may also start a sequence (no prior prefill: the forwards then
+ * ingest the forced tokens like a prompt, and out_tokens[0] is -1). Errors: INVALID (a dense model with
+ * non-NULL expert arguments, an expert id outside [0, n_experts)), and those of kie_decode_forced. */
+int kie_decode_forced_routed(kie_ctx *ctx, int n, const int32_t *forced, const int32_t *forced_experts,
+                             int32_t *out_tokens, float *out_logits, int32_t *out_experts);
+
+/* No counterpart on the pages (they sample on the device and never return logits): an inspection call.
+ * Copy the current logits (those the next emitted token is the argmax of) to host float[vocab]. */
 int kie_get_logits(kie_ctx *ctx, float *out);
 
-/* Number of tokens in the KV cache (the position the next forward writes). */
+/* No counterpart on the pages: sequence bookkeeping of this library.
+ * Number of tokens in the KV cache (the position the next forward writes). */
 int kie_position(const kie_ctx *ctx);
 
-/* Forget the sequence: position 0, no current logits. The KV cache is not cleared (it is overwritten). */
+/* No counterpart on the pages: sequence bookkeeping of this library.
+ * Forget the sequence: position 0, no current logits. The KV cache is not cleared (it is overwritten). */
 int kie_reset(kie_ctx *ctx);
 
 /* Device-side wait limit in nanoseconds for grid barriers and ring waits (default 1e9). */
@@ -177,12 +204,14 @@ int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, in
  * state carried in ctx), but allocates nothing: the per-launch scratch (activations, split-KV partials and
  * the control block) lives in one static device array of KIE_NOALLOC_SCRATCH_BYTES that every GPU loading
  * the library holds until the process exits. The caller passes the output: out_tokens_dev, n int32 in
- * DEVICE memory. The call is synchronous (it waits for the ctx stream) and returns KIE_OK, KIE_ERR_TIMEOUT,
- * or the errors of kie_decode; a model whose scratch exceeds the array is rejected with KIE_ERR_INVALID
- * (the message gives both sizes). The first call on a device looks up the array's device address (with
- * that device current), so make that first call before any stream capture. All calls share the one array
- * and it keeps the last call's contents (the control block is cleared by every call): calls that overlap
- * on the GPU, from any ctx on the same device, race with each other and must be serialised by the caller. */
+ * DEVICE memory. The device the ctx was created on must be the current device (KIE_ERR_INVALID otherwise).
+ * The call is synchronous (it waits for the ctx stream) and returns KIE_OK, KIE_ERR_TIMEOUT, or the errors of
+ * kie_decode; a model whose scratch exceeds the array is rejected with KIE_ERR_INVALID (the message gives both
+ * sizes). It takes the same launch path as kie_decode, so a kie_debug_skip_arrival armed before it applies to
+ * it. The first call on a device looks up the array's device address (with that device current), so make that
+ * first call before any stream capture. All calls share the one array and it keeps the last call's contents
+ * (the control block is cleared by every call): calls that overlap on the GPU, from any ctx on the same
+ * device, race with each other and must be serialised by the caller. */
 #define KIE_NOALLOC_SCRATCH_BYTES (512u * 1024u)
 int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
 

@@ -132,6 +132,7 @@ SIGNATURES = {
     "kie_decode_async": ([P, ctypes.c_int, P], ctypes.c_int),
     "kie_sync": ([P], ctypes.c_int),
     "kie_decode_forced": ([P, ctypes.c_int, P, P, P], ctypes.c_int),
+    "kie_decode_forced_routed": ([P, ctypes.c_int, P, P, P, P, P], ctypes.c_int),
     "kie_get_logits": ([P, P], ctypes.c_int),
     "kie_position": ([P], ctypes.c_int),
     "kie_reset": ([P], ctypes.c_int),
@@ -308,13 +309,25 @@ class Decoder:
         _check(lib().kie_decode(self.ctx, n, out.ctypes.data), self.ctx)
         return out
 
+    @staticmethod
+    def _device_tokens(out_dev, n: int) -> int:
+        """Address of out_dev after checking that it can take n int32 tokens written by the kernel: a contiguous
+        int32 CUDA tensor of at least n elements (the kernel writes n values there, unchecked)."""
+        torch = _torch()
+        if not isinstance(out_dev, torch.Tensor) or not out_dev.is_cuda:
+            raise ValueError("out_dev must be a CUDA tensor")
+        if out_dev.dtype != torch.int32 or not out_dev.is_contiguous() or out_dev.numel() < n:
+            raise ValueError(f"out_dev must be a contiguous int32 tensor of at least {n} elements "
+                             f"(got {out_dev.dtype}, {out_dev.numel()} elements, contiguous={out_dev.is_contiguous()})")
+        return out_dev.data_ptr()
+
     def decode_async(self, n: int, out_dev) -> None:
         """Enqueue n greedy tokens into the device int32 tensor out_dev; no synchronisation."""
-        _check(lib().kie_decode_async(self.ctx, n, out_dev.data_ptr()), self.ctx)
+        _check(lib().kie_decode_async(self.ctx, n, self._device_tokens(out_dev, n)), self.ctx)
 
     def decode_noalloc(self, n: int, out_dev) -> None:
         """n greedy tokens into the device int32 tensor out_dev, with no device allocation (static scratch)."""
-        _check(lib().kie_decode_noalloc(self.ctx, n, out_dev.data_ptr()), self.ctx)
+        _check(lib().kie_decode_noalloc(self.ctx, n, self._device_tokens(out_dev, n)), self.ctx)
 
     def sync(self) -> None:
         _check(lib().kie_sync(self.ctx), self.ctx)
@@ -326,6 +339,25 @@ class Decoder:
         _check(lib().kie_decode_forced(self.ctx, f.size, f.ctypes.data, toks.ctypes.data,
                                        logits.ctypes.data if want_logits else None), self.ctx)
         return toks, logits
+
+    def decode_forced_routed(self, forced, forced_experts=None, want_logits: bool = True, want_experts: bool = True):
+        """Teacher forcing of tokens and (sparse MoE) of expert selections: forced_experts [n, n_layers, top_k] or
+        None. Returns (tokens [n], logits [n, V] or None, own selections [n, n_layers, top_k] or None). May start a
+        sequence (then tokens[0] is -1)."""
+        f = np.ascontiguousarray(forced, dtype=np.int32)
+        n, L, k = f.size, self.model.n_layers, getattr(self.model, "top_k", 0)
+        toks = np.empty(n, dtype=np.int32)
+        logits = np.empty((n, self.model.vocab), dtype=np.float32) if want_logits else None
+        fe = None
+        if forced_experts is not None:
+            fe = np.ascontiguousarray(forced_experts, dtype=np.int32)
+            if fe.shape != (n, L, k):
+                raise ValueError(f"forced_experts must have shape {(n, L, k)}, not {fe.shape}")
+        own = np.empty((n, L, k), dtype=np.int32) if want_experts else None
+        _check(lib().kie_decode_forced_routed(self.ctx, n, f.ctypes.data, None if fe is None else fe.ctypes.data,
+                                              toks.ctypes.data, None if logits is None else logits.ctypes.data,
+                                              None if own is None else own.ctypes.data), self.ctx)
+        return toks, logits, own
 
     def logits(self) -> np.ndarray:
         out = np.empty(self.model.vocab, dtype=np.float32)

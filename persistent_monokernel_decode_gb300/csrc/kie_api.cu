@@ -44,9 +44,17 @@ struct WeightLayout {
       tc_layer_stride, tc_off[4], total;
 };
 
+// The per-launch scratch of the decode kernel: activations, router logits, split-KV partials and the control
+// block. It opens the ctx workspace; kie_decode_noalloc places the same layout in its static array instead.
+struct ScratchLayout {
+  size_t x, h, q, o, a, rlog, part_o, part_ml, ctl, total;
+};
+
 struct WsLayout {
-  size_t x, h, q, o, a, rlog, logits, part_o, part_ml, rope, ctl, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk,
-      pf_x, pf_h, pf_q, pf_o, pf_a, pf_scale, pf_part, pf_tcb, pf_att_o, pf_att_ml, total;
+  ScratchLayout scr;  // at offset 0
+  size_t logits, rope, persist, trace, trace_arrive, stats, tok_in, tok_out, chunk, route_in, route_out, pf_x, pf_h,
+      pf_q, pf_o, pf_a,
+      pf_scale, pf_part, pf_tcb, pf_att_o, pf_att_ml, total;
   int smax;
 };
 
@@ -59,6 +67,32 @@ struct Plan {
 };
 
 int max_rows_per_cta(int M, int n) { return 2 * ((M / 2 + n - 1) / n); }
+
+// Split-KV pieces per KV head at most: one CTA each.
+int split_kv_max(const kie_config *c, int n_cta) { return std::max(1, n_cta / c->n_kv_heads); }
+
+ScratchLayout scratch_layout(const kie_config *c, const kie_moe_config *moe, int n_cta) {
+  const int dq = c->n_heads * c->head_dim, G = c->n_heads / c->n_kv_heads, smax = split_kv_max(c, n_cta);
+  const int topk = moe ? moe->top_k : 0, E = moe ? moe->n_experts : 0;
+  ScratchLayout s;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += al(bytes);
+    return at;
+  };
+  s.x = take((size_t)c->d_model * 4);
+  s.h = take((size_t)c->d_model * 4);
+  s.q = take((size_t)dq * 4);
+  s.o = take((size_t)dq * 4);
+  s.a = take((size_t)c->ffn_dim * std::max(1, topk) * 4);
+  s.rlog = take((size_t)E * 4);
+  s.part_o = take((size_t)c->n_kv_heads * smax * G * c->head_dim * 4);
+  s.part_ml = take((size_t)c->n_kv_heads * smax * G * 2 * 4);
+  s.ctl = take(sizeof(kie::Ctl));
+  s.total = o;
+  return s;
+}
 
 const char *check_moe(const kie_config *c, const kie_moe_config *m) {
   if (!m) return nullptr;
@@ -151,24 +185,16 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   pl->kv_bytes = al(L * 2 * c->n_kv_heads * (size_t)c->max_seq * dh * 2);
   // workspace
   WsLayout &s = pl->ws;
-  s.smax = std::max(1, n_cta / c->n_kv_heads);
-  size_t o = 0;
+  s.smax = split_kv_max(c, n_cta);
+  s.scr = scratch_layout(c, moe, n_cta);
+  size_t o = s.scr.total;
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o += al(bytes);
     return at;
   };
-  s.x = take((size_t)d * 4);
-  s.h = take((size_t)d * 4);
-  s.q = take((size_t)dq * 4);
-  s.o = take((size_t)dq * 4);
-  s.a = take((size_t)std::max(F, topk * F) * 4);
-  s.rlog = take((size_t)E * 4);
   s.logits = take((size_t)c->vocab * 4);
-  s.part_o = take((size_t)c->n_kv_heads * s.smax * G * dh * 4);
-  s.part_ml = take((size_t)c->n_kv_heads * s.smax * G * 2 * 4);
   s.rope = take((size_t)c->max_seq * (dh / 2) * 8);
-  s.ctl = take(sizeof(kie::Ctl));
   s.persist = take(sizeof(kie::Persist));
   s.trace = take((size_t)kie::TRACE_CAP * n_cta * 4);
   s.trace_arrive = take((size_t)kie::TRACE_CAP * n_cta * 8);
@@ -176,6 +202,9 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   s.tok_in = take((size_t)c->max_seq * 4);
   s.tok_out = take((size_t)c->max_seq * 4);
   s.chunk = take((size_t)LOGIT_CHUNK * c->vocab * 4);
+  // forced and returned expert selections of one forced-decode launch (sparse MoE)
+  s.route_in = take((size_t)LOGIT_CHUNK * L * topk * 4);
+  s.route_out = take((size_t)LOGIT_CHUNK * L * topk * 4);
   // batched prefill: fp32 activations of one chunk of prompt tokens
   s.pf_x = take((size_t)kie::PF_TOKENS * d * 4);
   s.pf_h = take((size_t)kie::PF_TOKENS * d * 4);
@@ -217,6 +246,7 @@ bool device_info(DeviceInfo *di, std::string *err) {
 }  // namespace
 
 struct kie_ctx {
+  int device = -1;  // the CUDA device the ctx was created on (current at creation)
   kie_config cfg{};
   kie_moe_config moe{};  // n_experts == 0: dense FFN
   cudaStream_t stream = nullptr;
@@ -410,6 +440,19 @@ int upload_rope(kie_ctx *ctx) {
   return KIE_OK;
 }
 
+// Point the per-launch scratch of p at `base` laid out as `l`.
+void point_scratch(kie::DecodeParams &p, uint8_t *base, const ScratchLayout &l) {
+  p.x = (float *)(base + l.x);
+  p.h = (float *)(base + l.h);
+  p.q = (float *)(base + l.q);
+  p.o = (float *)(base + l.o);
+  p.a = (float *)(base + l.a);
+  p.rlog = (float *)(base + l.rlog);
+  p.part_o = (float *)(base + l.part_o);
+  p.part_ml = (float *)(base + l.part_ml);
+  p.ctl = (kie::Ctl *)(base + l.ctl);
+}
+
 void fill_base(kie_ctx *ctx) {
   const kie_config &c = ctx->cfg;
   const Plan &pl = ctx->plan;
@@ -452,17 +495,9 @@ void fill_base(kie_ctx *ctx) {
   p.kv = (__half *)ctx->kvbuf;
   uint8_t *ws = ctx->wsbuf;
   p.rope = (const float2 *)(ws + pl.ws.rope);
-  p.x = (float *)(ws + pl.ws.x);
-  p.h = (float *)(ws + pl.ws.h);
-  p.q = (float *)(ws + pl.ws.q);
-  p.o = (float *)(ws + pl.ws.o);
-  p.a = (float *)(ws + pl.ws.a);
-  p.rlog = (float *)(ws + pl.ws.rlog);
+  point_scratch(p, ws, pl.ws.scr);
   p.logits = (float *)(ws + pl.ws.logits);
-  p.part_o = (float *)(ws + pl.ws.part_o);
-  p.part_ml = (float *)(ws + pl.ws.part_ml);
   p.smax = pl.ws.smax;
-  p.ctl = (kie::Ctl *)(ws + pl.ws.ctl);
   p.persist = (kie::Persist *)(ws + pl.ws.persist);
   p.trace = (uint32_t *)(ws + pl.ws.trace);
   p.trace_arrive = (unsigned long long *)(ws + pl.ws.trace_arrive);
@@ -499,6 +534,7 @@ int create_common(const kie_config *cfg, const kie_moe_config *moe, const kie_we
   std::string err;
   if (!device_info(&di, &err)) return fail(nullptr, KIE_ERR_CUDA, err);
   kie_ctx *ctx = new kie_ctx();
+  ctx->device = di.dev;
   ctx->cfg = *cfg;
   if (moe) ctx->moe = *moe;
   ctx->stream = (cudaStream_t)stream;
@@ -551,10 +587,16 @@ int create_common(const kie_config *cfg, const kie_moe_config *moe, const kie_we
   return KIE_OK;
 }
 
-// One launch of the decode kernel. forced_dev / out_tokens_dev / out_logits_dev may be null.
+// One launch of the decode kernel. forced_dev / out_tokens_dev / out_logits_dev may be null. scratch: the
+// per-launch scratch (laid out by scratch_layout), or null for the ctx workspace's. route_in_dev / route_out_dev:
+// forced and returned expert selections ([n][L][top_k], sparse MoE), or null.
 int launch(kie_ctx *ctx, int n, int mode, int lm_last_only, const int *forced_dev, int *out_tokens_dev,
-           float *out_logits_dev) {
+           float *out_logits_dev, uint8_t *scratch = nullptr, const int *route_in_dev = nullptr,
+           int *route_out_dev = nullptr) {
   kie::DecodeParams p = ctx->base;
+  if (scratch) point_scratch(p, scratch, ctx->plan.ws.scr);
+  p.forced_experts = route_in_dev;
+  p.out_experts = route_out_dev;
   p.pos0 = ctx->pos;
   p.n = n;
   p.mode = mode;
@@ -567,7 +609,7 @@ int launch(kie_ctx *ctx, int n, int mode, int lm_last_only, const int *forced_de
   p.skip_barrier = ctx->skip_barrier;
   ctx->skip_cta = ctx->skip_barrier = -1;
   const Plan &pl = ctx->plan;
-  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + pl.ws.ctl, 0, sizeof(kie::Ctl), ctx->stream));
+  KIE_CUDA(ctx, cudaMemsetAsync(p.ctl, 0, sizeof(kie::Ctl), ctx->stream));
   KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + pl.ws.stats, 0, (size_t)pl.n_cta * 32, ctx->stream));
   cudaError_t e = kie_launch_decode(p, pl.smem, ctx->stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
@@ -579,11 +621,12 @@ int launch(kie_ctx *ctx, int n, int mode, int lm_last_only, const int *forced_de
   return KIE_OK;
 }
 
-// Wait for the stream and read the status word of the last launch.
-int finish(kie_ctx *ctx) {
+// Wait for the stream and read the status word of the last launch (whose scratch was `scratch`, or the ctx
+// workspace's when null).
+int finish(kie_ctx *ctx, uint8_t *scratch = nullptr) {
   int32_t *st = ctx->pinned + ctx->cfg.max_seq;
-  KIE_CUDA(ctx, cudaMemcpyAsync(st, ctx->wsbuf + ctx->plan.ws.ctl + offsetof(kie::Ctl, status), 8,
-                                cudaMemcpyDeviceToHost, ctx->stream));
+  const uint8_t *ctl = (scratch ? scratch : ctx->wsbuf) + ctx->plan.ws.scr.ctl;
+  KIE_CUDA(ctx, cudaMemcpyAsync(st, ctl + offsetof(kie::Ctl, status), 8, cudaMemcpyDeviceToHost, ctx->stream));
   KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
   if (st[0] != kie::ST_OK) {
     ctx->pos = 0;
@@ -682,7 +725,7 @@ int kie_prefill(kie_ctx *ctx, const int32_t *tokens, int n) {
                       ctx->wbuf + wl.tc, (long long)wl.tc_layer_stride,
                       {(long long)wl.tc_off[0], (long long)wl.tc_off[1], (long long)wl.tc_off[2], (long long)wl.tc_off[3]},
                       b + ws.pf_tcb, &ctx->base.ctl->status, ctx->timeout_ns};
-  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.ctl, 0, sizeof(kie::Ctl), ctx->stream));
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.scr.ctl, 0, sizeof(kie::Ctl), ctx->stream));
   const cudaError_t e = kie_run_prefill(ctx->base, pb, tin, ctx->pos, n, ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "prefill launch");
   ctx->pos += n;
@@ -716,32 +759,64 @@ int kie_decode(kie_ctx *ctx, int n, int32_t *out_tokens) {
   return rc;
 }
 
-int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_tokens, float *out_logits) {
+// Teacher-forced launches in chunks of LOGIT_CHUNK steps (the per-step logits of a chunk fit the workspace).
+// Without current logits (allowed only when allow_start is set) the first emitted token is undefined: -1.
+static int decode_forced_impl(kie_ctx *ctx, int n, const int32_t *forced, const int32_t *forced_experts,
+                              int32_t *out_tokens, float *out_logits, int32_t *out_experts, bool allow_start) {
   if (!ctx) return KIE_ERR_INVALID;
   if (n < 1 || !forced || !out_tokens) return fail(ctx, KIE_ERR_INVALID, "forced decode needs n >= 1 and buffers");
-  if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
+  if (!ctx->has_logits && !allow_start)
+    return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
   if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
   for (int i = 0; i < n; ++i)
     if (forced[i] < 0 || forced[i] >= ctx->cfg.vocab) return fail(ctx, KIE_ERR_INVALID, "token id out of range");
+  const int E = ctx->moe.n_experts, K = ctx->moe.top_k, L = ctx->cfg.n_layers;
+  if ((forced_experts || out_experts) && E == 0)
+    return fail(ctx, KIE_ERR_INVALID, "expert selections are given or asked for, but the model is dense");
+  if (forced_experts)
+    for (size_t i = 0; i < (size_t)n * L * K; ++i)
+      if (forced_experts[i] < 0 || forced_experts[i] >= E) return fail(ctx, KIE_ERR_INVALID, "expert id out of range");
+  const bool fresh = !ctx->has_logits;
   const int V = ctx->cfg.vocab;
+  const size_t per_step = (size_t)L * K;  // expert ids per forward
   int *tin = (int *)(ctx->wsbuf + ctx->plan.ws.tok_in);
   int *tout = (int *)(ctx->wsbuf + ctx->plan.ws.tok_out);
   float *chunk = (float *)(ctx->wsbuf + ctx->plan.ws.chunk);
+  int *rin = (int *)(ctx->wsbuf + ctx->plan.ws.route_in);
+  int *rout = (int *)(ctx->wsbuf + ctx->plan.ws.route_out);
   for (int done = 0; done < n;) {
     const int m = std::min(LOGIT_CHUNK, n - done);
     std::memcpy(ctx->pinned, forced + done, (size_t)m * 4);
     KIE_CUDA(ctx, cudaMemcpyAsync(tin, ctx->pinned, (size_t)m * 4, cudaMemcpyHostToDevice, ctx->stream));
-    int rc = launch(ctx, m, kie::MODE_FORCED, 0, tin, tout, out_logits ? chunk : nullptr);
+    if (forced_experts)
+      KIE_CUDA(ctx, cudaMemcpyAsync(rin, forced_experts + (size_t)done * per_step, (size_t)m * per_step * 4,
+                                    cudaMemcpyHostToDevice, ctx->stream));
+    int rc = launch(ctx, m, kie::MODE_FORCED, 0, tin, tout, out_logits ? chunk : nullptr, nullptr,
+                    forced_experts ? rin : nullptr, out_experts ? rout : nullptr);
     if (rc != KIE_OK) return rc;
     KIE_CUDA(ctx, cudaMemcpyAsync(out_tokens + done, tout, (size_t)m * 4, cudaMemcpyDeviceToHost, ctx->stream));
     if (out_logits)
       KIE_CUDA(ctx, cudaMemcpyAsync(out_logits + (size_t)done * V, chunk, (size_t)m * V * 4, cudaMemcpyDeviceToHost,
                                     ctx->stream));
+    if (out_experts)
+      KIE_CUDA(ctx, cudaMemcpyAsync(out_experts + (size_t)done * per_step, rout, (size_t)m * per_step * 4,
+                                    cudaMemcpyDeviceToHost, ctx->stream));
     rc = finish(ctx);
     if (rc != KIE_OK) return rc;
+    ctx->has_logits = true;
     done += m;
   }
+  if (fresh) out_tokens[0] = -1;
   return KIE_OK;
+}
+
+int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_tokens, float *out_logits) {
+  return decode_forced_impl(ctx, n, forced, nullptr, out_tokens, out_logits, nullptr, false);
+}
+
+int kie_decode_forced_routed(kie_ctx *ctx, int n, const int32_t *forced, const int32_t *forced_experts,
+                             int32_t *out_tokens, float *out_logits, int32_t *out_experts) {
+  return decode_forced_impl(ctx, n, forced, forced_experts, out_tokens, out_logits, out_experts, true);
 }
 
 int kie_get_logits(kie_ctx *ctx, float *out) {
@@ -902,11 +977,12 @@ int kie_rows_of_cta(int M, int n_cta, int cta, int *r0, int *r1) {
 
 // ---- decode without device allocation ---------------------------------------------------------------------
 //
-// kie_decode_noalloc runs the same kernel as kie_decode, but the per-launch scratch (activations, split-KV
-// partials and the control block) lives in the static array below instead of the ctx workspace. Nothing in
-// this path allocates device or host memory. The array is a file-scope __device__ object, so each GPU that
-// loads the library holds KIE_NOALLOC_SCRATCH_BYTES of it until the process exits; host code never uses its
-// name as an address, only the device address that cudaGetSymbolAddress returns for the current device.
+// kie_decode_noalloc runs the same kernel through the same launch path as kie_decode, but the per-launch scratch
+// (activations, split-KV partials and the control block, laid out by scratch_layout) lives in the static array
+// below instead of the ctx workspace. Nothing in this path allocates device or host memory. The array is a
+// file-scope __device__ object, so each GPU that loads the library holds KIE_NOALLOC_SCRATCH_BYTES of it until the
+// process exits; host code never uses its name as an address, only the device address that cudaGetSymbolAddress
+// returns for the ctx's device (which must be current).
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[KIE_NOALLOC_SCRATCH_BYTES];
 
@@ -916,37 +992,16 @@ constexpr int NOALLOC_MAX_DEVICES = 64;
 void *g_noalloc_addr[NOALLOC_MAX_DEVICES];  // device address of g_noalloc_scratch per device (null: not set up)
 std::mutex g_noalloc_mutex;
 
-struct NoallocLayout {
-  size_t x, h, q, o, a, rlog, part_o, part_ml, ctl, total;
-};
-
-NoallocLayout noalloc_layout(const kie_config &c, const kie_moe_config &moe, const Plan &pl) {
-  const int pl_topk = moe.top_k, pl_experts = moe.n_experts;
-  const int dq = c.n_heads * c.head_dim, G = c.n_heads / c.n_kv_heads;
-  NoallocLayout s;
-  size_t o = 0;
-  auto take = [&](size_t bytes) {
-    const size_t at = o;
-    o += al(bytes);
-    return at;
-  };
-  s.x = take((size_t)c.d_model * 4);
-  s.h = take((size_t)c.d_model * 4);
-  s.q = take((size_t)dq * 4);
-  s.o = take((size_t)dq * 4);
-  s.a = take((size_t)c.ffn_dim * std::max(1, pl_topk) * 4);
-  s.rlog = take((size_t)pl_experts * 4);
-  s.part_o = take((size_t)c.n_kv_heads * pl.ws.smax * G * c.head_dim * 4);
-  s.part_ml = take((size_t)c.n_kv_heads * pl.ws.smax * G * 2 * 4);
-  s.ctl = take(sizeof(kie::Ctl));
-  s.total = o;
-  return s;
-}
-
 // Once per device, with that device current: the device address of the static scratch array.
 int noalloc_scratch(kie_ctx *ctx, uint8_t **out) {
   int dev = 0;
   KIE_CUDA(ctx, cudaGetDevice(&dev));
+  if (dev != ctx->device) {
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "kie_decode_noalloc: the ctx's device %d must be current (device %d is)",
+                  ctx->device, dev);
+    return fail(ctx, KIE_ERR_INVALID, buf);
+  }
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(ctx, KIE_ERR_INVALID, "device ordinal out of range");
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (!g_noalloc_addr[dev]) {
@@ -966,54 +1021,20 @@ extern "C" int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev) 
   if (n < 1 || !out_tokens_dev) return fail(ctx, KIE_ERR_INVALID, "decode needs n >= 1 and an output buffer");
   if (!ctx->has_logits) return fail(ctx, KIE_ERR_INVALID, "decode before prefill: there are no current logits");
   if ((long long)ctx->pos + n > ctx->cfg.max_seq) return fail(ctx, KIE_ERR_CAPACITY, "decode exceeds max_seq");
-  const NoallocLayout lay = noalloc_layout(ctx->cfg, ctx->moe, ctx->plan);
-  if (lay.total > KIE_NOALLOC_SCRATCH_BYTES) {
+  const size_t need = ctx->plan.ws.scr.total;
+  if (need > KIE_NOALLOC_SCRATCH_BYTES) {
     char buf[200];
     std::snprintf(buf, sizeof buf,
                   "this model needs %zu bytes of decode scratch; the static scratch of kie_decode_noalloc holds %u",
-                  lay.total, (unsigned)KIE_NOALLOC_SCRATCH_BYTES);
+                  need, (unsigned)KIE_NOALLOC_SCRATCH_BYTES);
     return fail(ctx, KIE_ERR_INVALID, buf);
   }
   uint8_t *scr = nullptr;
   int rc = noalloc_scratch(ctx, &scr);
   if (rc != KIE_OK) return rc;
-  kie::DecodeParams p = ctx->base;
-  p.x = (float *)(scr + lay.x);
-  p.h = (float *)(scr + lay.h);
-  p.q = (float *)(scr + lay.q);
-  p.o = (float *)(scr + lay.o);
-  p.a = (float *)(scr + lay.a);
-  p.rlog = (float *)(scr + lay.rlog);
-  p.part_o = (float *)(scr + lay.part_o);
-  p.part_ml = (float *)(scr + lay.part_ml);
-  p.ctl = (kie::Ctl *)(scr + lay.ctl);
-  p.pos0 = ctx->pos;
-  p.n = n;
-  p.mode = kie::MODE_DECODE;
-  p.lm_last_only = 0;
-  p.forced = nullptr;
-  p.out_tokens = out_tokens_dev;
-  p.out_logits = nullptr;
-  p.timeout_ns = ctx->timeout_ns;
-  p.skip_cta = p.skip_barrier = -1;
-  // The control block must start at zero; the array keeps whatever the previous call left in it.
-  KIE_CUDA(ctx, cudaMemsetAsync(scr + lay.ctl, 0, sizeof(kie::Ctl), ctx->stream));
-  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + ctx->plan.ws.stats, 0, (size_t)ctx->plan.n_cta * 32, ctx->stream));
-  const cudaError_t e = kie_launch_decode(p, ctx->plan.smem, ctx->stream);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    cudaGetLastError();
-    return fail(ctx, KIE_ERR_LAUNCH, "cooperative launch refused: the grid cannot be co-resident");
-  }
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "decode kernel launch");
-  ctx->pos += n;
-  int32_t *st = ctx->pinned + ctx->cfg.max_seq;
-  KIE_CUDA(ctx, cudaMemcpyAsync(st, scr + lay.ctl + offsetof(kie::Ctl, status), 8, cudaMemcpyDeviceToHost,
-                                ctx->stream));
-  KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));
-  if (st[0] != kie::ST_OK) {
-    ctx->pos = 0;
-    ctx->has_logits = false;
-    return fail(ctx, KIE_ERR_TIMEOUT, "device wait timed out; sequence reset");
-  }
-  return KIE_OK;
+  // launch() clears the control block (the array keeps whatever the previous call left in it) and takes any
+  // armed kie_debug_skip_arrival, like every other launch
+  rc = launch(ctx, n, kie::MODE_DECODE, 0, nullptr, out_tokens_dev, nullptr, scr);
+  if (rc != KIE_OK) return rc;
+  return finish(ctx, scr);
 }

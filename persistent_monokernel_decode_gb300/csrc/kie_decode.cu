@@ -402,8 +402,9 @@ __device__ inline void moe_router(const DecodeParams &p, Smem &s, int l, float i
 // Every CTA, after the router barrier: the top_k largest logits (the lowest id first among equal ones), in
 // descending order, and the softmax over them; warp 0 computes it (all CTAs get identical results from identical
 // inputs), publishes it to the producer through the selection mbarrier, and every consumer sees it after the
-// closing consumer_sync.
-__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel) {
+// closing consumer_sync. With p.forced_experts the given experts of (token t, layer l) are used instead of the
+// own selection (which still goes to p.out_experts).
+__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel, int t, int l) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     constexpr int PER = MAX_EXPERTS / 32;
@@ -429,6 +430,9 @@ __device__ inline void moe_select(const DecodeParams &p, const Smem &s, const Mo
         if (lane + 32 * i == id) key[i] = 0ull;
       if (lane == j) mine = id;
     }
+    const size_t at = ((size_t)t * p.L + l) * p.top_k + lane;
+    if (p.out_experts && blockIdx.x == 0 && lane < p.top_k) p.out_experts[at] = mine;
+    if (p.forced_experts && lane < p.top_k) mine = p.forced_experts[at];  // ids checked on the host
     const float v = lane < p.top_k ? __ldcg(p.rlog + mine) : -INFINITY;
     const float mx = warp_max(v);
     const float ev = lane < p.top_k ? expf(v - mx) : 0.f;
@@ -579,7 +583,7 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
         moe_router(p, s, l, inv);
         if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
         const MoeSel sel = moe_sel(p, s);
-        moe_select(p, s, sel);
+        moe_select(p, s, sel, t, l);
         // row scales of this CTA's rows of the routed experts, copied while the first tiles are in flight
         const int Re = rg.r1 - rg.r0, Rd = ro.r1 - ro.r0;
         float *const scg = s.out + p.out_moe + MOE_SEL_FLOATS, *const scd = scg + p.top_k * Re;

@@ -71,6 +71,11 @@ struct DecodeParams {
   long long off_router, off_egu, off_edn, off_esgu, off_esdn, egu_bytes, edn_bytes;
   const float *gffn;  // [L][d] FFN RMSNorm gains (fp32), applied to the staged vector (FP8 weights keep them out)
   float *rlog;        // [E] router logits of the current layer
+  // testing aids (device, or null): forced_experts [n][L][top_k] replaces each layer's own top_k selection (the
+  // routing weights are still the softmax of this launch's router logits over the given experts); out_experts
+  // [n][L][top_k] receives the kernel's own selection, in selection order
+  const int *forced_experts;
+  int *out_experts;
 };
 
 }  // namespace kie

@@ -200,6 +200,26 @@ def test_prefill_attention_pieces_are_independent_of_the_cut(kie):
     dec.close()
 
 
+def test_forced_decode_can_start_a_sequence(tiny, kie):
+    """kie_decode_forced_routed without a prior prefill ingests the forced tokens like a prompt (the first emitted
+    token is -1); afterwards it is an ordinary teacher-forced decode, and expert arguments are refused for a dense
+    model."""
+    w, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    ref_tokens, ref_logits = oracle.generate(TINY, w, prompt, 6, max_seq=dec.max_seq)
+    dec.reset()
+    toks, logits, own = dec.decode_forced_routed(np.concatenate([prompt, ref_tokens]), want_experts=False)
+    assert toks[0] == -1 and own is None
+    P = len(prompt)
+    assert float(np.max(np.abs(logits[P - 1:] - ref_logits))) <= LOGIT_TOL
+    sure = margins(ref_logits[:-1]) > MARGIN
+    assert np.array_equal(toks[P:][sure], ref_tokens[sure])
+    dec.reset()
+    with pytest.raises(kie.KieError) as e:
+        dec.decode_forced_routed(prompt, want_experts=True)
+    assert e.value.code == kie.KIE_ERR_INVALID
+
+
 def test_api_errors(tiny, kie):
     _, dec = tiny
     dec.reset()
@@ -297,6 +317,27 @@ def test_context_with_an_empty_split_kv_piece(kie):
     dec.close()
 
 
+# ---- long context at the 2B widths -------------------------------------------------------------------------
+
+def test_long_context_at_2b_widths(kie):
+    """The long-context workload's shape on two layers: the 2B widths (d 2,560, 20 query heads of 128 over 4 KV
+    heads, F 7,680, vocab 32,000), a prompt of 8,192 ids, then 8 teacher-forced decode steps against the oracle.
+    The prefill runs the tensor-core attention with groups of 5 query heads over 16 pieces of 512 positions and
+    their merge; every decode step splits about 8,200 positions over 38 pieces per KV head of several 32-position
+    sub-chunks each (the oracle takes a couple of minutes on the host cores)."""
+    cfg = dataclasses.replace(TWO_B, name="llama2b_L2", n_layers=2)
+    w = synth.model_weights(cfg)
+    prompt = synth.tokens(TWO_B.seed, 8192, cfg.vocab)
+    dec = kie.Decoder(cfg, w, max_seq=8192 + 8)
+    try:
+        smax = max(1, dec.n_cta // cfg.n_kv_heads)
+        S, C = split_kv(8193, smax)
+        assert C > 32, "the decode steps must give each piece several sub-chunks"
+        check_run(dec, cfg, w, prompt, 8, 8192 + 8)
+    finally:
+        dec.close()
+
+
 # ---- the 2B workload at full size, in the launch configuration the bench times ---------------------------
 
 @pytest.fixture(scope="module")
@@ -307,11 +348,12 @@ def two_b(kie):
     dec.close()
 
 
-def test_2b_sampled_steps_match_oracle(two_b):
-    """Prompt of 128 ids and the first 8 teacher-forced decode steps of the 2B model, against the oracle."""
+def test_2b_every_decode_step_matches_oracle(two_b):
+    """The bench workload in full: the 2B model, prompt of 128 ids, and all 1,024 decode steps teacher-forced
+    against the oracle, logits compared at every step (the oracle takes a few minutes on the host cores)."""
     w, dec = two_b
     prompt = synth.tokens(TWO_B.seed, 128, TWO_B.vocab)
-    check_run(dec, TWO_B, w, prompt, 8, 128 + 1024)
+    check_run(dec, TWO_B, w, prompt, 1024, 128 + 1024)
 
 
 def test_2b_full_decode_properties(two_b):

@@ -69,6 +69,21 @@ def test_noalloc_matches_decode_sparse_moe(kie):
     two_calls_each_way(kie, MOE_TINY, synth.tokens(MOE_TINY.seed, 10, MOE_TINY.vocab), 6, 5, 32)
 
 
+def test_noalloc_checks_the_output_tensor(kie):
+    """The binding refuses an output tensor the kernel could write past: wrong dtype, too short, on the host."""
+    import torch
+    dec = kie.Decoder(TINY, synth.model_weights(TINY), max_seq=32)
+    try:
+        dec.prefill([1, 2, 3])
+        for bad in (torch.empty(4, dtype=torch.int64, device="cuda"), torch.empty(3, dtype=torch.int32, device="cuda"),
+                    torch.empty(4, dtype=torch.int32), torch.empty(8, dtype=torch.int32, device="cuda")[::2]):
+            with pytest.raises(ValueError):
+                dec.decode_noalloc(4, bad)
+        assert dec.position == 3
+    finally:
+        dec.close()
+
+
 def test_noalloc_and_regular_calls_interleave(kie):
     import torch
     w = synth.model_weights(TINY)
@@ -88,12 +103,49 @@ def test_noalloc_and_regular_calls_interleave(kie):
         dec.close()
 
 
+def test_noalloc_wait_limit_then_a_clean_decode(kie):
+    """A grid-barrier arrival skipped on purpose (host-side hook, no GPU fault) during a no-allocation decode: the
+    bounded waits run out, the call reports KIE_ERR_TIMEOUT from the static array's control block, and the ctx
+    then decodes correctly again (teacher-forced against the oracle)."""
+    import torch
+
+    import oracle
+    w = synth.model_weights(TINY)
+    prompt = synth.prompt(TINY_DECODE)
+    dec = kie.Decoder(TINY, w, max_seq=64)
+    try:
+        dec.prefill(prompt)
+        dec.set_timeout_ns(20_000_000)
+        dec.debug_skip_arrival(cta=3, barrier=2)
+        out = torch.empty(4, dtype=torch.int32, device="cuda")
+        with pytest.raises(kie.KieError) as e:
+            dec.decode_noalloc(4, out)
+        assert e.value.code == kie.KIE_ERR_TIMEOUT
+        assert dec.position == 0  # a timed-out launch resets the sequence
+        dec.set_timeout_ns(1_000_000_000)
+        ref_tokens, ref_logits = oracle.generate(TINY, w, prompt, 8, max_seq=64)
+        dec.prefill(prompt)
+        toks, logits = dec.decode_forced(ref_tokens)
+        assert np.max(np.abs(logits - ref_logits[1:])) <= LOGIT_TOL
+        # and the skip was consumed by the timed-out call: a no-allocation decode now runs to the end
+        dec.reset()
+        dec.prefill(prompt)
+        dec.decode_noalloc(4, out)
+        assert dec.position == len(prompt) + 4
+    finally:
+        dec.close()
+
+
 def test_noalloc_rejects_scratch_beyond_the_static_array(kie):
-    # eight query heads of 128 on one KV head: the split-KV partials alone exceed the array
+    # eight query heads of 128 on one KV head: the split-KV partials, one per CTA of the grid, take n_cta * 8 * 128
+    # * 4 bytes, more than the 512 KB array from about 128 CTAs on (152 on GB300)
     cfg = ModelConfig("big", n_layers=1, d_model=256, n_heads=8, n_kv_heads=1, head_dim=128, ffn_dim=256,
                       vocab=256, seed=3)
     import torch
     dec = kie.Decoder(cfg, synth.model_weights(cfg), max_seq=16)
+    if dec.n_cta * 8 * 128 * 4 <= 512 * 1024:
+        dec.close()
+        pytest.skip(f"with {dec.n_cta} CTAs this model's scratch fits the static array")
     try:
         dec.prefill([1, 2, 3])
         out = torch.empty(2, dtype=torch.int32, device="cuda")
