@@ -86,12 +86,13 @@ def phase_breakdown(dec, model, prompt_len, new):
     stamps = np.unique(arrive)
     step = float(np.min(np.diff(stamps))) if stamps.size > 1 else 0.0
     out = {"tokens": f"{toks} tokens from c = {prompt_len + 1}", "timer_step_ns": step,
-           "note": "%globaltimer stamps advance in timer_step_ns steps: each phase median is quantised to it",
-           "release_latency_us": float(np.median(release)),
-           "barrier_us_per_token": float(np.median(release)) * per_tok}
+           "note": "%globaltimer stamps advance in timer_step_ns steps: a single phase time is quantised to it; "
+                   "us is the mean over the recorded phases, median_us the (quantised) median",
+           "release_latency_us": float(np.mean(release)),
+           "barrier_us_per_token": float(np.mean(release)) * per_tok}
     for n, v in per.items():
-        us = float(np.median(v))
-        out[n] = {"us": us, "gbs": b[n] / us / 1e3}
+        us = float(np.mean(v))  # the mean over many phases is finer than one timer step
+        out[n] = {"us": us, "gbs": b[n] / us / 1e3, "median_us": float(np.median(v))}
     return out
 
 
@@ -363,6 +364,45 @@ def prefill_bench(args):
           flush=True)
 
 
+def attention_phase(args):
+    """The decode's split-KV attention step alone (kie_profile_attention: the same device function and grid
+    barrier), on a 2-layer model of the 2B widths with the cache filled to c = 145 and c = 8,192 positions: time per
+    layer (CUDA events over --steps launches, median) and the K/V bytes it must read (2 x Hkv x dh x c fp16 per
+    layer), as one JSON line per context."""
+    import dataclasses
+
+    import torch
+
+    import persistent_monokernel_decode_gb300 as kie
+    import synth
+    from synth.configs import TWO_B
+    kie.build()
+    layers = 2
+    model = dataclasses.replace(TWO_B, name="llama2b_L2", n_layers=layers)
+    w = synth.model_weights(model)
+    peaks, peak_kind = measured_peaks()
+    for c in (145, 8192):
+        dec = kie.Decoder(model, w, max_seq=c + 8)
+        dec.prefill(synth.tokens(model.seed, c, model.vocab))
+        times = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(dec.stream)
+            dec.profile_attention(c, layers)
+            e1.record(dec.stream)
+            torch.cuda.synchronize()
+            if i >= args.warmup:
+                times.append(e0.elapsed_time(e1) / 1e3)
+        t_layer = statistics.median(times) / layers
+        kv = 2 * 2 * model.n_kv_heads * model.head_dim * c
+        print(json.dumps({"metric": "split-KV attention step alone, per layer", "c": c, "us_per_layer": t_layer * 1e6,
+                          "kv_bytes_per_layer": kv, "GBs": kv / t_layer / 1e9, "frac_of_peak": kv / t_layer / 1e9 / peaks["hbm_gbs"],
+                          "peak_kind": peak_kind, "launch": f"{layers} layers per launch, includes one grid barrier per layer",
+                          "steps": args.steps, "warmup": args.warmup}), flush=True)
+        dec.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -379,6 +419,8 @@ def main():
     ap.add_argument("--moe", action="store_true",
                     help="the sparse-MoE workload (64 FP8 experts, top 4): prompt 256, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
+    ap.add_argument("--phase-attention", action="store_true",
+                    help="the decode's split-KV attention step alone at c = 145 and 8,192 (2 layers of the 2B widths)")
     ap.add_argument("--phase-gemv", action="store_true",
                     help="the decode's five projection shapes of the 2B model through the standalone GEMV (GB/s each)")
     args = ap.parse_args()
@@ -389,6 +431,9 @@ def main():
         args.decode = 512 if args.decode == NEW else args.decode
     if args.gemv_sweep:
         gemv_sweep(args)
+        return
+    if args.phase_attention:
+        attention_phase(args)
         return
     if args.phase_gemv:
         gemv_sweep(args, phase_shapes(), "2B decode projection as one standalone GEMV: GB/s (cold HBM, CUDA graph)")
@@ -468,7 +513,7 @@ def main():
     clk = clocks.stop()
     stats = dec.barrier_stats()
     phases = phase_breakdown(dec, model, prompt_len, new)
-    step_s = max_over_ranks(sum(times) / len(times), pg)
+    step_s = max_over_ranks(statistics.median(times), pg)
     value = replica_throughput(world, new, step_s)
 
     # end to end through the host-buffer API: reset + prefill(host prompt) + decode(n, host tokens)
@@ -483,7 +528,7 @@ def main():
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             e2e_times.append(dt)
-    e2e_step = max_over_ranks(sum(e2e_times) / len(e2e_times), pg)
+    e2e_step = max_over_ranks(statistics.median(e2e_times), pg)
 
     peaks, peak_kind = measured_peaks()
     bytes_launch = algorithmic_bytes(model, prompt_len, new)
@@ -501,6 +546,9 @@ def main():
         "e2e": {"value": replica_throughput(world, new, e2e_step), "unit": "tok/s", "h2d_bytes_per_step": prompt_len * 4,
                 "d2h_bytes_per_step": new * 4 + 8,
                 "timed": f"reset + prefill({prompt_len}-token host prompt) + decode({new} -> host array), wall clock"},
+        "statistic": f"median over the {args.steps} timed launches (CUDA events on the library's stream), "
+                     "max over ranks",
+        "step_ms_all": [round(1e3 * t, 4) for t in times],
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": frac, "traffic": profiled_traffic(workload, kie.source_digest()),

@@ -174,6 +174,14 @@ int kie_get_barrier_trace(kie_ctx *ctx, int first, int count, uint64_t *arrive_n
  * returns KIE_ERR_TIMEOUT after the configured limit. No GPU fault, trap or unbounded wait is involved. */
 int kie_debug_skip_arrival(kie_ctx *ctx, int cta, int barrier);
 
+/* No counterpart on the pages: a profiling aid. Runs the decode kernel's split-KV attention step alone (the same
+ * device function and grid barrier, one cooperative launch) for layers [0, n_layers) over c cached positions,
+ * with the q vector and K/V cache the ctx currently holds, so that a profiler can measure that phase's DRAM bytes
+ * and time in isolation. Writes only the attention outputs and split-KV partials of the workspace; the sequence
+ * (position, current logits, KV cache) is left as it was. Synchronous. Errors: INVALID (c outside [1, max_seq],
+ * n_layers outside [1, n_layers]), CUDA, LAUNCH, TIMEOUT. */
+int kie_profile_attention(kie_ctx *ctx, int c, int n_layers);
+
 int kie_n_cta(const kie_ctx *ctx);
 const char *kie_last_error(const kie_ctx *ctx); /* ctx may be NULL: last error of a failed create */
 void kie_destroy(kie_ctx *ctx);

@@ -141,6 +141,7 @@ SIGNATURES = {
     "kie_get_barrier_trace": ([P, ctypes.c_int, ctypes.c_int, P, P], ctypes.c_int),
     "kie_debug_skip_arrival": ([P, ctypes.c_int, ctypes.c_int], ctypes.c_int),
     "kie_n_cta": ([P], ctypes.c_int),
+    "kie_profile_attention": ([P, ctypes.c_int, ctypes.c_int], ctypes.c_int),
     "kie_last_error": ([P], ctypes.c_char_p),
     "kie_destroy": ([P], None),
     "kie_gemv_packed_bytes": ([ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
@@ -388,6 +389,10 @@ class Decoder:
         if m < 0:
             _check(m, self.ctx)
         return arrive[:m], wait[:m]
+
+    def profile_attention(self, c: int, n_layers: int) -> None:
+        """The split-KV attention step alone for layers [0, n_layers) over c cached positions (profiling)."""
+        _check(lib().kie_profile_attention(self.ctx, c, n_layers), self.ctx)
 
     def debug_skip_arrival(self, cta: int, barrier: int) -> None:
         _check(lib().kie_debug_skip_arrival(self.ctx, cta, barrier), self.ctx)

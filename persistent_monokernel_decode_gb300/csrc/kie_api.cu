@@ -17,6 +17,7 @@
 
 cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream);
 int kie_decode_max_blocks_per_sm(size_t smem);
+cudaError_t kie_launch_attention(const kie::DecodeParams &p, size_t smem, int c, int n_layers, cudaStream_t stream);
 cudaError_t kie_launch_gemv(const uint8_t *packed, const __half *x, float *y, int M, int K, int n_cta, int nslot,
                             unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t kie_launch_pack(const uint16_t *src, uint16_t *dst, int M, int K, int n_cta, const uint16_t *gain,
@@ -901,6 +902,31 @@ int kie_debug_skip_arrival(kie_ctx *ctx, int cta, int barrier) {
   ctx->skip_cta = cta;
   ctx->skip_barrier = barrier;
   return KIE_OK;
+}
+
+int kie_profile_attention(kie_ctx *ctx, int c, int n_layers) {
+  if (!ctx) return KIE_ERR_INVALID;
+  if (c < 1 || c > ctx->cfg.max_seq || n_layers < 1 || n_layers > ctx->cfg.n_layers)
+    return fail(ctx, KIE_ERR_INVALID, "profile_attention needs 1 <= c <= max_seq and 1 <= n_layers <= n_layers");
+  kie::DecodeParams p = ctx->base;
+  p.timeout_ns = ctx->timeout_ns;
+  const Plan &pl = ctx->plan;
+  KIE_CUDA(ctx, cudaMemsetAsync(p.ctl, 0, sizeof(kie::Ctl), ctx->stream));
+  KIE_CUDA(ctx, cudaMemsetAsync(ctx->wsbuf + pl.ws.stats, 0, (size_t)pl.n_cta * 32, ctx->stream));
+  const cudaError_t e = kie_launch_attention(p, pl.smem, c, n_layers, ctx->stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return fail(ctx, KIE_ERR_LAUNCH, "cooperative launch refused: the grid cannot be co-resident");
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "attention kernel launch");
+  const bool had = ctx->has_logits;
+  const int pos = ctx->pos;
+  const int rc = finish(ctx);
+  if (rc == KIE_OK) {  // the sequence is untouched (the step writes only the attention outputs and partials)
+    ctx->has_logits = had;
+    ctx->pos = pos;
+  }
+  return rc;
 }
 
 int kie_n_cta(const kie_ctx *ctx) { return ctx ? ctx->plan.n_cta : KIE_ERR_INVALID; }

@@ -698,7 +698,50 @@ __global__ void __launch_bounds__(BLOCK, 1) decode_kernel(const DecodeParams p) 
   consumer_main<MOE>(p, s, g);
 }
 
+// The split-KV attention step alone (profiling): layers [0, n_layers) over c cached positions, with whatever q and
+// cache the workspace holds, through the same device function and grid barrier as decode_kernel. The producer
+// warp has nothing to stream and leaves after the ring set-up.
+__global__ void __launch_bounds__(BLOCK, 1) attention_kernel(const DecodeParams p, int c, int n_layers) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem s = carve_smem(smem_raw, p.nslot, p.vec_floats, p.out_floats);
+  init_ring(s, p.nslot);
+  const Guard g{&p.ctl->status, p.timeout_ns};
+  if (threadIdx.x >= NCT) return;
+  uint32_t gen = 0;
+  unsigned att_target = 0;
+  unsigned long long wait_ns = 0;
+  const uint64_t t_start = globaltimer();
+  for (int l = 0; l < n_layers; ++l) {
+    const int S = split_pieces(p, c), C = (c + S - 1) / S;
+    att_target += (unsigned)S;
+    if ((int)blockIdx.x < p.Hkv * S) {
+      const int kh = blockIdx.x / S, sp = blockIdx.x % S;
+      const int j0 = min(c, sp * C), j1 = min(c, j0 + C);
+      if (p.dh == 128)
+        attention_piece<4>(p, s, l, kh, sp, S, j0, j1, att_target, g);
+      else
+        attention_piece<2>(p, s, l, kh, sp, S, j0, j1, att_target, g);
+    }
+    if (!grid_barrier(p, s, gen, g, wait_ns)) break;
+  }
+  if (threadIdx.x == 0) {
+    unsigned long long *st = p.cta_stats + (size_t)blockIdx.x * 4;
+    st[0] = wait_ns;
+    st[1] = gen;
+    st[2] = t_start;
+    st[3] = globaltimer();
+  }
+}
+
 }  // namespace kie
+
+cudaError_t kie_launch_attention(const kie::DecodeParams &p, size_t smem, int c, int n_layers, cudaStream_t stream) {
+  const void *fn = (const void *)kie::attention_kernel;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void *args[] = {(void *)&p, (void *)&c, (void *)&n_layers};
+  return cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kie::BLOCK), args, smem, stream);
+}
 
 // Launch helper used by the C ABI (kie_api.cu).
 cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream) {

@@ -220,6 +220,22 @@ def test_forced_decode_can_start_a_sequence(tiny, kie):
     assert e.value.code == kie.KIE_ERR_INVALID
 
 
+def test_profile_attention_leaves_the_sequence_alone(tiny):
+    """The attention step run alone (profiling) changes neither the position nor the current logits, and decode
+    afterwards still matches the oracle."""
+    w, dec = tiny
+    prompt = synth.prompt(TINY_DECODE)
+    dec.reset()
+    dec.prefill(prompt)
+    before = dec.logits()
+    dec.profile_attention(len(prompt), TINY.n_layers)
+    assert dec.position == len(prompt)
+    np.testing.assert_array_equal(dec.logits(), before)
+    ref_tokens, ref_logits = oracle.generate(TINY, w, prompt, 4, max_seq=dec.max_seq)
+    _, logits = dec.decode_forced(ref_tokens)
+    assert float(np.max(np.abs(logits - ref_logits[1:]))) <= LOGIT_TOL
+
+
 def test_api_errors(tiny, kie):
     _, dec = tiny
     dec.reset()
