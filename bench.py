@@ -366,41 +366,39 @@ def prefill_bench(args):
 
 def attention_phase(args):
     """The decode's split-KV attention step alone (kie_profile_attention: the same device function and grid
-    barrier), on a 2-layer model of the 2B widths with the cache filled to c = 145 and c = 8,192 positions: time per
-    layer (CUDA events over --steps launches, median) and the K/V bytes it must read (2 x Hkv x dh x c fp16 per
-    layer), as one JSON line per context."""
-    import dataclasses
-
+    barrier), on the 2B model with its cache filled to c positions: the step's time per layer from the kernel's
+    own clock (first CTA start to end, 25 layers per launch, so the launch itself is not in it; median over
+    --steps launches) and the K/V bytes it must read (2 x Hkv x dh x c fp16 per layer), one JSON line per c."""
     import torch
 
     import persistent_monokernel_decode_gb300 as kie
     import synth
     from synth.configs import TWO_B
     kie.build()
-    layers = 2
-    model = dataclasses.replace(TWO_B, name="llama2b_L2", n_layers=layers)
+    model = TWO_B
+    layers = model.n_layers
     w = synth.model_weights(model)
     peaks, peak_kind = measured_peaks()
-    for c in (145, 8192):
-        dec = kie.Decoder(model, w, max_seq=c + 8)
+    cs = (129, 145, 300, 600, 1152, 8192)
+    dec = kie.Decoder(model, w, max_seq=max(cs) + 8)
+    del w
+    for c in cs:
+        dec.reset()
         dec.prefill(synth.tokens(model.seed, c, model.vocab))
         times = []
         for i in range(args.warmup + args.steps):
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(dec.stream)
             dec.profile_attention(c, layers)
-            e1.record(dec.stream)
             torch.cuda.synchronize()
             if i >= args.warmup:
-                times.append(e0.elapsed_time(e1) / 1e3)
+                times.append(dec.barrier_stats()["total_ns"] * 1e-9)
         t_layer = statistics.median(times) / layers
         kv = 2 * 2 * model.n_kv_heads * model.head_dim * c
         print(json.dumps({"metric": "split-KV attention step alone, per layer", "c": c, "us_per_layer": t_layer * 1e6,
-                          "kv_bytes_per_layer": kv, "GBs": kv / t_layer / 1e9, "frac_of_peak": kv / t_layer / 1e9 / peaks["hbm_gbs"],
-                          "peak_kind": peak_kind, "launch": f"{layers} layers per launch, includes one grid barrier per layer",
+                          "kv_bytes_per_layer": kv, "GBs": kv / t_layer / 1e9,
+                          "frac_of_peak": kv / t_layer / 1e9 / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                          "timing": f"kernel clock over {layers} layers per launch, one grid barrier per layer",
                           "steps": args.steps, "warmup": args.warmup}), flush=True)
-        dec.close()
+    dec.close()
 
 
 def main():
@@ -420,7 +418,7 @@ def main():
                     help="the sparse-MoE workload (64 FP8 experts, top 4): prompt 256, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
     ap.add_argument("--phase-attention", action="store_true",
-                    help="the decode's split-KV attention step alone at c = 145 and 8,192 (2 layers of the 2B widths)")
+                    help="the decode's split-KV attention step alone, 2B model, c from 129 to 8,192")
     ap.add_argument("--phase-gemv", action="store_true",
                     help="the decode's five projection shapes of the 2B model through the standalone GEMV (GB/s each)")
     args = ap.parse_args()
