@@ -369,17 +369,19 @@ def attention_phase(args):
     barrier), on the 2B model with its cache filled to c positions: the step's time per layer from the kernel's
     own clock (first CTA start to end, 25 layers per launch, so the launch itself is not in it; median over
     --steps launches) and the K/V bytes it must read (2 x Hkv x dh x c fp16 per layer), one JSON line per c."""
+    import dataclasses
+
     import torch
 
     import persistent_monokernel_decode_gb300 as kie
     import synth
     from synth.configs import TWO_B
     kie.build()
-    model = TWO_B
+    model = TWO_B if args.layers == TWO_B.n_layers else dataclasses.replace(TWO_B, n_layers=args.layers)
     layers = model.n_layers
     w = synth.model_weights(model)
     peaks, peak_kind = measured_peaks()
-    cs = (129, 145, 300, 600, 1152, 8192)
+    cs = tuple(int(v) for v in args.contexts.split(","))
     dec = kie.Decoder(model, w, max_seq=max(cs) + 8)
     del w
     for c in cs:
@@ -393,7 +395,8 @@ def attention_phase(args):
                 times.append(dec.barrier_stats()["total_ns"] * 1e-9)
         t_layer = statistics.median(times) / layers
         kv = 2 * 2 * model.n_kv_heads * model.head_dim * c
-        print(json.dumps({"metric": "split-KV attention step alone, per layer", "c": c, "us_per_layer": t_layer * 1e6,
+        print(json.dumps({"metric": "split-KV attention step alone, per layer", "c": c, "layers": layers,
+                          "us_per_layer": t_layer * 1e6,
                           "kv_bytes_per_layer": kv, "GBs": kv / t_layer / 1e9,
                           "frac_of_peak": kv / t_layer / 1e9 / peaks["hbm_gbs"], "peak_kind": peak_kind,
                           "timing": f"kernel clock over {layers} layers per launch, one grid barrier per layer",
@@ -417,6 +420,8 @@ def main():
     ap.add_argument("--moe", action="store_true",
                     help="the sparse-MoE workload (64 FP8 experts, top 4): prompt 256, 512 new tokens")
     ap.add_argument("--gemv-sweep", action="store_true", help="standalone GEMV GB/s for the 25 sweep shapes")
+    ap.add_argument("--contexts", default="129,145,300,600,1152,8192",
+                    help="attended positions for --phase-attention, comma-separated")
     ap.add_argument("--phase-attention", action="store_true",
                     help="the decode's split-KV attention step alone, 2B model, c from 129 to 8,192")
     ap.add_argument("--phase-gemv", action="store_true",

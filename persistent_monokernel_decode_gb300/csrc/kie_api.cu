@@ -126,10 +126,12 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   pl->n_cta = n_cta;
   if (n_cta < c->n_kv_heads) return "the grid needs at least one CTA per KV head";
   // shared memory: ring + input vector (largest of d, F, Hq*dh, attention scratch) + row results
-  // attention scratch (floats): q [G][dh] f32, K and V sub-chunks [ATT_SUB][dh] f16, scores [G][ATT_SUB],
-  // 3 x MAX_GROUP running values, and the merge's [smax][G] m/weight and l arrays
+  // attention scratch (floats): the q operand [16][dh + 8] f16, K and V sub-chunks [ATT_SUB][dh + 8] f16,
+  // scores [MAX_GROUP][ATT_SUB], the P operand [16][ATT_SUB + 8] f16, 3 x MAX_GROUP running values, and the
+  // merge's [smax][G] m/weight and l arrays
   const int smax = std::max(1, n_cta / c->n_kv_heads);
-  const int att = G * dh + kie::ATT_SUB * dh + G * kie::ATT_SUB + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
+  const int att = 8 * (dh + 8) + kie::ATT_SUB * (dh + 8) + kie::MAX_GROUP * kie::ATT_SUB +
+                  8 * (kie::ATT_SUB + 8) + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
   pl->vec_floats = std::max(std::max(std::max(d, c->ffn_dim), std::max(dq, att)), topk * F);
   // row results of the widest projection (for MoE also top_k experts' rows side by side), then this CTA's slices
   // of x and h, then the token's RoPE row, then (MoE) the expert selection and the routed experts' row scales

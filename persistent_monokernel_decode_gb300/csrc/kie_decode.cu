@@ -122,21 +122,35 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
 // Latency matters more than bandwidth here (a piece reads <= 16 KB of K/V per sub-chunk), so every sub-chunk's
 // K and V rows are requested together with q in one round trip, the next sub-chunk is prefetched into registers
 // while the current one is used from shared memory, and no step waits on a dependent global load.
+//
+// Both products of a sub-chunk run on the tensor cores (mma.sync m16n8k16, fp32 accumulation): the scores as
+// Q K^T with the group's query heads as the rows of A, then O += P V. K and V are fp16 already, so they are
+// exact operands; q and the softmax weights p are fp32, and each is split into an fp16 high part and the fp16
+// rounding of the remainder, which fill rows h and 8 + h of A. The two rows' products are summed in fp32, so
+// the result carries about 22 significant bits of q and p instead of fp16's 11.
 template <int DPL>
 __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, int kh, int sp, int S, int j0,
                                        int j1, unsigned target, const Guard &g) {
   constexpr int DH = DPL * 32;
   constexpr int U = DH / 8;                          // 16-byte units per K or V row
   constexpr int UPT = (ATT_SUB * U + NCT - 1) / NCT;  // units per thread per sub-chunk
-  static_assert(ATT_SUB == 32, "one lane per position of a sub-chunk");
-  static_assert(MAX_GROUP <= NCW, "one consumer warp per query head of a group");
+  constexpr int RS = DH + 8;                         // row stride (halfs) of q, K and V: 16-byte rows that
+                                                     // ldmatrix reads from eight different bank groups
+  constexpr int PS = ATT_SUB + 8;                    // row stride (halfs) of P
+  constexpr int NTILE = DH / 8;                      // 8-column tiles of the output
+  constexpr int TPW = (NTILE + NCW - 1) / NCW;       // output tiles per consumer warp
+  static_assert(ATT_SUB == 32, "four 8-position score tiles, two 16-position P V steps per sub-chunk");
+  static_assert(MAX_GROUP <= 8, "a group's high parts fill rows 0..7 of A, the low parts rows 8..15");
+  static_assert(MAX_GROUP <= NCW, "one consumer warp per query head in the softmax");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int fg = lane >> 2, ft = lane & 3;           // fragment row group and column pair of this lane
   const int G = p.Hq / p.Hkv;
-  float *qs = s.vec;                                   // [G][DH], pre-scaled by 1/sqrt(dh)
-  __half *Ks = reinterpret_cast<__half *>(qs + G * DH);  // [ATT_SUB][DH]
-  __half *Vs = Ks + ATT_SUB * DH;                      // [ATT_SUB][DH]
-  float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * DH);  // [G][ATT_SUB]
-  float *corr = ps + G * ATT_SUB;                      // [MAX_GROUP]
+  __half *qA = reinterpret_cast<__half *>(s.vec);    // [16][RS] q / sqrt(dh): high parts, low parts
+  __half *Ks = qA + 16 * RS;                         // [ATT_SUB][RS]
+  __half *Vs = Ks + ATT_SUB * RS;                    // [ATT_SUB][RS]
+  float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * RS);  // [MAX_GROUP][ATT_SUB] scores
+  __half *PA = reinterpret_cast<__half *>(ps + MAX_GROUP * ATT_SUB);  // [16][PS] p: high parts, low parts
+  float *corr = reinterpret_cast<float *>(PA + 16 * PS);  // [MAX_GROUP]
   float *mrun = corr + MAX_GROUP;
   float *lrun = mrun + MAX_GROUP;
   float *mw = lrun + MAX_GROUP;                        // merge: [smax][G] m, then weights
@@ -159,10 +173,8 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       }
     }
   };
-  // shared memory <- the registers fetched for jb; rows past the end are zero, so that the score and P.V loops
-  // below can always run over ATT_SUB positions without guards. K rows are stored swizzled: 16-byte chunk c
-  // of row j sits at chunk c ^ (j % U), so the score loop (one lane per row, all lanes on chunk c) reads
-  // eight different bank groups per quarter warp.
+  // shared memory <- the registers fetched for jb; rows past the end are zero, so that both products below
+  // always run over ATT_SUB positions (a zero V row times a zero weight adds nothing)
   auto stash = [&](int jb) {
     const int nb = min(ATT_SUB, j1 - jb);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -171,97 +183,110 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
       const int u = tid + k * NCT;
       if (u < ATT_SUB * U) {
         const bool in = u < nb * U;
-        const int row = u / U, c = u % U;
-        *reinterpret_cast<uint4 *>(Ks + (size_t)row * DH + (size_t)(c ^ (row % U)) * 8) = in ? kreg[k] : zero;
-        *reinterpret_cast<uint4 *>(Vs + (size_t)u * 8) = in ? vreg[k] : zero;
+        const size_t at = (size_t)(u / U) * RS + (u % U) * 8;
+        *reinterpret_cast<uint4 *>(Ks + at) = in ? kreg[k] : zero;
+        *reinterpret_cast<uint4 *>(Vs + at) = in ? vreg[k] : zero;
       }
     }
   };
 
   if (j0 < j1) fetch(j0);
-  for (int i = tid; i < G * DH; i += NCT) qs[i] = __ldcg(p.q + (size_t)kh * G * DH + i) * scale;
+  // A of the scores: row h = fp16(q_h), row 8 + h = fp16(q_h - row h); rows of heads past the group are zero
+  for (int i = tid; i < 16 * DH; i += NCT) {
+    const int r = i / DH, d = i % DH, h = r & 7;
+    float v = 0.f;
+    if (h < G) {
+      const float qv = __ldcg(p.q + ((size_t)kh * G + h) * DH + d) * scale;
+      const float hi = __half2float(__float2half_rn(qv));
+      v = r < 8 ? hi : qv - hi;
+    }
+    qA[r * RS + d] = __float2half_rn(v);
+  }
+  for (int i = tid; i < 16 * PS; i += NCT) PA[i] = __float2half_rn(0.f);
   if (tid < MAX_GROUP) {
     mrun[tid] = -INFINITY;
     lrun[tid] = 0.f;
   }
-  // each thread owns output pairs (h, d), (h, d + 1): o[k] for pair index tid + k * NCT
-  constexpr int OPT = (MAX_GROUP * DH / 2 + NCT - 1) / NCT;
-  float2 o[OPT];
+  // output accumulators: warp w owns column tiles w, w + NCW, ...; rows fg (high) and fg + 8 (low) of each
+  // belong to query head fg and are summed when the piece is published
+  float acc[TPW][4];
 #pragma unroll
-  for (int k = 0; k < OPT; ++k) o[k] = make_float2(0.f, 0.f);
+  for (int i = 0; i < TPW; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  // ldmatrix row addresses: lane l points at row (l % 8) + 8 * ((l / 8) % 2), column half l / 16 of A
+  const int arow = (lane & 7) + 8 * ((lane >> 3) & 1), acol = 8 * (lane >> 4);
 
   for (int jb = j0; jb < j1; jb += ATT_SUB) {
     const int nb = min(ATT_SUB, j1 - jb);
     stash(jb);
-    consumer_sync();                               // Ks, Vs (and qs) ready; ps free
+    consumer_sync();                               // Ks, Vs (and qA, PA) ready; ps free
     if (jb + ATT_SUB < j1) fetch(jb + ATT_SUB);    // next sub-chunk in flight while this one is used
-    // scores and the online-softmax update: warp h owns query head h, lane j position jb + j of the sub-chunk
-    // (a whole DH-long dot product per lane, no cross-lane sums); positions past nb weigh 0
+    // scores: warp w < 4 takes positions [8w, 8w + 8) of the sub-chunk over DH / 16 steps of 16
+    if (warp < ATT_SUB / 8) {
+      const int n0 = warp * 8;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < DH / 16; ++ks) {
+        uint32_t a[4], b[2];
+        ldsm_x4(a, qA + arow * RS + ks * 16 + acol);
+        ldsm_x2(b, Ks + (n0 + (lane & 7)) * RS + ks * 16 + 8 * ((lane >> 3) & 1));
+        mma_f16_f32(c, a, b);
+      }
+      if (fg < G)
+        *reinterpret_cast<float2 *>(ps + fg * ATT_SUB + n0 + 2 * ft) = make_float2(c[0] + c[2], c[1] + c[3]);
+    }
+    consumer_sync();
+    // online-softmax update: warp h owns query head h, lane j position jb + j; positions past nb weigh 0
     if (warp < G) {
       const int h = warp, jj = lane;
-      const float4 *qh = reinterpret_cast<const float4 *>(qs + h * DH);
-      const __half *kr = Ks + (size_t)jj * DH;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 4
-      for (int c = 0; c < U; ++c) {
-        const uint4 raw = *reinterpret_cast<const uint4 *>(kr + (c ^ (jj % U)) * 8);
-        const float4 qa = qh[2 * c], qb = qh[2 * c + 1];
-        const float2 k0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-        const float2 k1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-        const float2 k2 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.z));
-        const float2 k3 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.w));
-        a0 = fmaf(k0.x, qa.x, a0);
-        a1 = fmaf(k0.y, qa.y, a1);
-        a2 = fmaf(k1.x, qa.z, a2);
-        a3 = fmaf(k1.y, qa.w, a3);
-        a0 = fmaf(k2.x, qb.x, a0);
-        a1 = fmaf(k2.y, qb.y, a1);
-        a2 = fmaf(k3.x, qb.z, a2);
-        a3 = fmaf(k3.y, qb.w, a3);
-      }
-      const float sc = jj < nb ? (a0 + a1) + (a2 + a3) : -INFINITY;
+      const float sc = jj < nb ? ps[h * ATT_SUB + jj] : -INFINITY;
       const float mnew = fmaxf(mrun[h], warp_max(sc));
       const float e = jj < nb ? expf(sc - mnew) : 0.f;
-      ps[h * ATT_SUB + jj] = e;
+      const __half hi = __float2half_rn(e);
+      PA[h * PS + jj] = hi;
+      PA[(8 + h) * PS + jj] = __float2half_rn(e - __half2float(hi));
       const float sum = warp_sum(e);
       if (lane == 0) {
-        const float c = expf(mrun[h] - mnew);
-        corr[h] = c;
-        lrun[h] = lrun[h] * c + sum;
+        const float cr = expf(mrun[h] - mnew);
+        corr[h] = cr;
+        lrun[h] = lrun[h] * cr + sum;
         mrun[h] = mnew;
       }
     }
     consumer_sync();
-    // o = o * corr + P V over this sub-chunk: a fixed ATT_SUB steps (zero rows past nb), 4 independent sums
+    // o = o * corr + P V: two steps of 16 positions per column tile
+    {
+      const float cg = fg < G ? corr[fg] : 0.f;
+      uint32_t a0[4], a1[4];
+      ldsm_x4(a0, PA + arow * PS + acol);
+      ldsm_x4(a1, PA + arow * PS + 16 + acol);
 #pragma unroll
-    for (int k = 0; k < OPT; ++k) {
-      const int pr = tid + k * NCT;
-      if (pr < G * DH / 2) {
-        const int h = (2 * pr) / DH, d = (2 * pr) % DH;
-        const float *ph = ps + h * ATT_SUB;
-        float2 a[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      for (int i = 0; i < TPW; ++i) {
+        const int nt = warp + i * NCW;
+        if (nt < NTILE) {
 #pragma unroll
-        for (int jj = 0; jj < ATT_SUB; ++jj) {
-          const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(Vs + (size_t)jj * DH + d));
-          const float pj = ph[jj];
-          a[jj & 3].x = fmaf(pj, v.x, a[jj & 3].x);
-          a[jj & 3].y = fmaf(pj, v.y, a[jj & 3].y);
+          for (int e = 0; e < 4; ++e) acc[i][e] *= cg;
+          uint32_t b0[2], b1[2];
+          ldsm_x2_trans(b0, Vs + (lane & 15) * RS + nt * 8);
+          ldsm_x2_trans(b1, Vs + (16 + (lane & 15)) * RS + nt * 8);
+          mma_f16_f32(acc[i], a0, b0);
+          mma_f16_f32(acc[i], a1, b1);
         }
-        const float c = corr[h];
-        o[k].x = o[k].x * c + ((a[0].x + a[1].x) + (a[2].x + a[3].x));
-        o[k].y = o[k].y * c + ((a[0].y + a[1].y) + (a[2].y + a[3].y));
       }
     }
-    consumer_sync();                               // Ks, Vs, ps reused by the next sub-chunk
+    consumer_sync();                               // Ks, Vs, ps, PA reused by the next sub-chunk
   }
 
   // publish (m, l, o) of this piece
   const int E = G * DH;  // outputs of this KV head's query group
   const size_t piece = (size_t)kh * p.smax + sp;
+  if (fg < G) {
 #pragma unroll
-  for (int k = 0; k < OPT; ++k) {
-    const int pr = tid + k * NCT;
-    if (pr < E / 2) *reinterpret_cast<float2 *>(p.part_o + piece * E + 2 * pr) = o[k];
+    for (int i = 0; i < TPW; ++i) {
+      const int nt = warp + i * NCW;
+      if (nt < NTILE)
+        *reinterpret_cast<float2 *>(p.part_o + piece * E + (size_t)fg * DH + nt * 8 + 2 * ft) =
+            make_float2(acc[i][0] + acc[i][2], acc[i][1] + acc[i][3]);
+    }
   }
   if (tid < G) *reinterpret_cast<float2 *>(p.part_ml + (piece * G + tid) * 2) = make_float2(mrun[tid], lrun[tid]);
   consumer_sync();

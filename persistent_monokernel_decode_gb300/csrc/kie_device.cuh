@@ -121,6 +121,45 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// ---- warp-level tensor-core fragments (mma.sync m16n8k16, fp16 inputs, fp32 accumulators) -----------------
+//
+// Fragment ownership (g = lane / 4, t = lane % 4): A (16 x 16, row-major) a0 = rows g, cols 2t..2t+1;
+// a1 = row g + 8; a2 = row g, cols + 8; a3 = row g + 8, cols + 8. B (16 x 8, k x n) b0 = k 2t..2t+1, n g;
+// b1 = k + 8. C/D (16 x 8) c0, c1 = row g, cols 2t, 2t + 1; c2, c3 = row g + 8, same cols.
+
+// Four 8x8 fp16 matrices from shared memory; lanes 8i..8i+7 give the row addresses of matrix i (16-byte rows).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row))
+               : "memory");
+}
+
+// Two 8x8 fp16 matrices (lanes 0..15 give the row addresses; the others' are not used).
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(row))
+               : "memory");
+}
+
+// As ldsm_x2, each matrix transposed on the way (row-major k x n storage -> the B fragment).
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t (&r)[2], const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(row))
+               : "memory");
+}
+
+// d += A B on one 16x8x16 tile (registers only: the compiler may schedule it freely).
+__device__ __forceinline__ void mma_f16_f32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // ---- shared memory ---------------------------------------------------------------------------------------
 
 struct Smem {
