@@ -267,7 +267,9 @@ int kie_create_moe_with_buffers(const kie_config *cfg, const kie_moe_config *moe
                                 kie_ctx **out);
 
 /* Host-side layout query (no GPU needed): byte offset of code Q[r][c] inside a packed FP8 matrix [M, K]
- * (column blocks of 512 codes). M even, K a multiple of 16; -1 for bad arguments. */
+ * (column blocks of 512 codes, each CTA's rows in tiles of up to 32 rows; within a full 512-code block the
+ * 16-code chunk q of an odd row r is stored at chunk q ^ 4). M even, K a multiple of 16; -1 for bad
+ * arguments. */
 int64_t kie_packed_offset_fp8(int M, int K, int n_cta, int r, int c);
 
 /* Host-side layout query (no GPU needed): byte offset of W[r][c] inside the prefill's tensor-core copy of an

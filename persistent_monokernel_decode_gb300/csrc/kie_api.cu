@@ -133,6 +133,9 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
   const int att = 8 * (dh + 8) + kie::ATT_SUB * (dh + 8) + kie::MAX_GROUP * kie::ATT_SUB +
                   8 * (kie::ATT_SUB + 8) + 3 * kie::MAX_GROUP + 2 * smax * G + 64;
   pl->vec_floats = std::max(std::max(std::max(d, c->ffn_dim), std::max(dq, att)), topk * F);
+  // sparse MoE: the expert GEMVs' fp16 split of their input (g o h after its fp32 copy: 2d floats in all;
+  // a: top_k F floats) and their cross-warp partial sums (9 x TILE_ROWS floats)
+  if (moe) pl->vec_floats = std::max(pl->vec_floats, std::max(2 * d, topk * F) + kie::FP8_RED_FLOATS);
   // row results of the widest projection (for MoE also top_k experts' rows side by side), then this CTA's slices
   // of x and h, then the token's RoPE row, then (MoE) the expert selection and the routed experts' row scales
   const int rows_gu = max_rows_per_cta(2 * F, n_cta), rows_d = max_rows_per_cta(d, n_cta);
@@ -985,7 +988,7 @@ int kie_gemv(const uint16_t *packed_dev, const uint16_t *x_dev, float *y_dev, in
 
 int64_t kie_packed_offset_fp8(int M, int K, int n_cta, int r, int c) {
   if (M < 2 || M % 2 || K < 16 || K % 16 || n_cta < 1 || r < 0 || r >= M || c < 0 || c >= K) return -1;
-  return kie::packed_offset_bw(M, K, n_cta, r, c, kie::FP8_TILE_COLS);
+  return kie::packed_offset_fp8(M, K, n_cta, r, c);
 }
 
 int64_t kie_packed_offset(int M, int K, int n_cta, int r, int c) {

@@ -602,8 +602,10 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
       if constexpr (MOE) {
-        // [ROUTER] logits of u = inv_rms(h) * (g o h); the staged g o h stays for the experts
-        ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d);
+        // [ROUTER] logits of u = inv_rms(h) * (g o h); the staged g o h stays for the experts, also split into
+        // fp16 high and low parts (after the fp32 copy) for their tensor-core GEMVs
+        __half *const xgu = reinterpret_cast<__half *>(s.vec + p.d);
+        ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d, xgu);
         const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
         moe_router(p, s, l, inv);
         if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
@@ -624,7 +626,8 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
         // two experts per tile when stacked (see the producer): their rows land side by side in s.out
         const int step = (Re > 0 && 2 * Re <= TILE_ROWS) ? 2 : 1;
         for (int j = 0; j < p.top_k; j += step)
-          consume_region_fp8(s, p.nslot, rp, min(step, p.top_k - j) * Re, p.d, s.vec, inv, s.out + j * Re, g);
+          consume_region_fp8(s, p.nslot, rp, min(step, p.top_k - j) * Re, p.d, xgu, xgu + p.d, inv, s.out + j * Re,
+                             s.vec + 2 * p.d, g);
         cp_async_wait_all();
         consumer_sync();
         for (int i = tid; i < p.top_k * (Re / 2); i += NCT) {
@@ -636,9 +639,13 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
         if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
         // [EXPERT DOWN] x = h + sum_j w_j * (Wd_j a_j)
-        stage_f32(s, p.a, p.top_k * p.F, false);
+        // (a_j staged as fp16 high parts [top_k][F] then low parts [top_k][F])
+        __half *const xdn = reinterpret_cast<__half *>(s.vec);
+        const int KA = p.top_k * p.F;
+        stage_split(p.a, KA, xdn);
         for (int j = 0; j < p.top_k; ++j)
-          consume_region_fp8(s, p.nslot, rp, Rd, p.F, s.vec + (size_t)j * p.F, 1.0f, s.out + j * Rd, g);
+          consume_region_fp8(s, p.nslot, rp, Rd, p.F, xdn + (size_t)j * p.F, xdn + KA + (size_t)j * p.F, 1.0f,
+                             s.out + j * Rd, s.vec + KA, g);
         consumer_sync();
         for (int i = tid; i < Rd; i += NCT) {
           float acc = 0.f;

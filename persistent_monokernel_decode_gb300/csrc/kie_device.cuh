@@ -22,6 +22,7 @@ constexpr int NCW = 8;                          // consumer warps
 constexpr int NCT = NCW * 32;                   // consumer threads
 constexpr int BLOCK = NCT + 32;                 // + one producer warp
 constexpr int ROWS_PER_WARP = TILE_ROWS / NCW;  // rows of a tile each consumer warp owns
+constexpr int FP8_RED_FLOATS = (NCW + 1) * TILE_ROWS;  // partial sums of one FP8 row group
 static_assert(TILE_ROWS % NCW == 0, "tile rows must split evenly over consumer warps");
 
 constexpr int ST_OK = 0;
@@ -473,43 +474,110 @@ __device__ __forceinline__ float dot16_e4m3(const uint4 w, const float4 x0, cons
   return a + b;
 }
 
-// tile_loop for FP8 tiles: full FP8_TILE_COLS-wide column blocks, one 16-code chunk per lane and row.
-template <int NJ>
-__device__ __forceinline__ void tile_loop_fp8(const uint8_t *ring, uint64_t *full, uint64_t *empty, const float *vec,
-                                              float (&acc)[ROWS_PER_WARP], int nslot, int &slot, uint32_t &phase,
-                                              int k_end, bool &ok, volatile int *flags, const Guard &g) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Two E4M3 codes (the low and high byte of v) -> f16x2 (low half = low byte); exact, every E4M3 value is an
+// fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// x (fp32, 16 values from an fp16 high part and an fp16 low part) for the scalar path of ragged blocks.
+__device__ __forceinline__ void load_split16(const __half *xh, const __half *xl, float4 (&x)[4]) {
+  const uint4 h0 = *reinterpret_cast<const uint4 *>(xh), h1 = *reinterpret_cast<const uint4 *>(xh + 8);
+  const uint4 l0 = *reinterpret_cast<const uint4 *>(xl), l1 = *reinterpret_cast<const uint4 *>(xl + 8);
+  const uint32_t hw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+  const uint32_t lw[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&hw[i]));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2 *>(&lw[i]));
+    f[2 * i] = a.x + c.x;
+    f[2 * i + 1] = a.y + c.y;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+}
+
+// One full 512-code FP8 block of a row group on the tensor cores (mma.sync m16n8k16, fp32 accumulation).
+// A = the weights (E4M3 -> fp16, exact); B = x as two columns, its fp16 high part (column 0) and the fp16
+// rounding of the remainder (column 1); the other six columns are zero. The k order inside a 16-wide MMA step
+// is permuted so that a lane's four A values of a row are four consecutive codes: in step j of 64-code group q,
+// lane (g = lane / 4, t = lane % 4) holds codes 64q + 16t + 4j + {0, 1} (the fragment's k = 2t, 2t + 1) and
+// + {2, 3} (k = 2t + 8, 2t + 9), and B is read in the same order. NMB row blocks of 16: with NMB = 2 warp w
+// takes rows 16 (w % 2) + [0, 16) and groups w / 2, w / 2 + 4; with NMB = 1 every warp takes rows [0, 16) and
+// group w. `wa`, `wb`: the lane's 16-byte chunks of rows g and g + 8 of its row block, per group.
+template <int NMB>
+__device__ __forceinline__ void fp8_block_mma(const uint4 (&wa)[NMB], const uint4 (&wb)[NMB], const __half *xh,
+                                              const __half *xl, int k0, float (&acc)[4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, fg = lane >> 2, ft = lane & 3;
+#pragma unroll
+  for (int i = 0; i < NMB; ++i) {
+    const int grp = NMB == 2 ? (warp >> 1) + 4 * i : warp;
+    uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+    if (fg < 2) {
+      const __half *xs = (fg == 0 ? xh : xl) + k0 + grp * 64 + ft * 16;
+      x0 = *reinterpret_cast<const uint4 *>(xs);
+      x1 = *reinterpret_cast<const uint4 *>(xs + 8);
+    }
+    const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    const uint32_t ww[4] = {wa[i].x, wa[i].y, wa[i].z, wa[i].w};
+    const uint32_t vw[4] = {wb[i].x, wb[i].y, wb[i].z, wb[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t a[4] = {e4m3x2_to_f16x2(ww[j]), e4m3x2_to_f16x2(vw[j]), e4m3x2_to_f16x2(ww[j] >> 16),
+                             e4m3x2_to_f16x2(vw[j] >> 16)};
+      const uint32_t b[2] = {xw[2 * j], xw[2 * j + 1]};
+      mma_f16_f32(acc, a, b);
+    }
+  }
+}
+
+// The full blocks of one row group (rows <= TILE_ROWS) for NMB row blocks of 16; every warp waits for and
+// releases every tile (the ring's empty barriers count NCW arrivals), after copying its chunks to registers.
+template <int NMB>
+__device__ __forceinline__ void tile_loop_fp8_mma(const uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                                  const __half *xh, const __half *xl, float (&acc)[4], int nslot,
+                                                  int &slot, uint32_t &phase, int k_end, bool &ok,
+                                                  volatile int *flags, const Guard &g) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, fg = lane >> 2, ft = lane & 3;
+  const int ra = (NMB == 2 ? 16 * (warp & 1) : 0) + fg;  // rows ra and ra + 8 (same parity)
+  const uint32_t swz = (uint32_t)(ra & 1) << 6;          // chunk q of an odd row is stored at q ^ 4
   for (int k0 = 0; k0 < k_end; k0 += FP8_TILE_COLS) {
     if (ok && !wait_mbar(&full[slot], phase, g)) {
       ok = false;
       flags[0] = 1;
     }
-    uint4 wv[NJ > 0 ? NJ : 1];
-    const uint8_t *t = ring + (size_t)slot * SLOT_BYTES + (size_t)warp * FP8_TILE_COLS + lane * 16;
+    const uint8_t *tile = ring + (size_t)slot * SLOT_BYTES;
+    uint4 wa[NMB], wb[NMB];
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) wv[j] = *reinterpret_cast<const uint4 *>(t + (size_t)j * NCW * FP8_TILE_COLS);
+    for (int i = 0; i < NMB; ++i) {
+      const int grp = NMB == 2 ? (warp >> 1) + 4 * i : warp;
+      const uint32_t cb = ((uint32_t)(grp * 64 + ft * 16)) ^ swz;
+      wa[i] = *reinterpret_cast<const uint4 *>(tile + (size_t)ra * FP8_TILE_COLS + cb);
+      wb[i] = *reinterpret_cast<const uint4 *>(tile + (size_t)(ra + 8) * FP8_TILE_COLS + cb);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     if (++slot == nslot) {
       slot = 0;
       phase ^= 1u;
     }
-    if (NJ > 0) {
-      const float4 *xv = reinterpret_cast<const float4 *>(vec + k0 + lane * 16);
-      const float4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
-#pragma unroll
-      for (int j = 0; j < NJ; ++j) acc[j] += dot16_e4m3(wv[j], x0, x1, x2, x3);
-    }
+    fp8_block_mma<NMB>(wa, wb, xh, xl, k0, acc);
   }
 }
 
-// out[i] = scale * sum_k Q[r0 + i][k] * vec[k] over the R rows of this CTA in one packed FP8 region (codes
-// taken at their E4M3 value; the caller applies the row scales). Same tile walk, warp/row ownership and abort
-// behaviour as consume_region; K is a multiple of 16.
+// out[i] = scale * sum_k Q[r0 + i][k] * x[k] over the R rows of this CTA in one packed FP8 region (codes taken at
+// their E4M3 value; the caller applies the row scales). x is given as its fp16 high part xh and low part xl
+// (K values each). Full 512-code blocks run on the tensor cores (fp8_block_mma); a ragged last block takes the
+// CUDA-core path with x = xh + xl, one 16-code chunk per lane and row, rows warp, warp + NCW, ... Per row group
+// the partial sums meet in `red` (9 x TILE_ROWS floats) and are added in a fixed order. A thread whose wait
+// gives up raises the CTA abort flag and walks the same tile sequence, like consume_region.
 static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingPos &rp, int R, int K,
-                                                       const float *vec, float scale, float *out, const Guard &g) {
+                                                       const __half *xh, const __half *xl, float scale,
+                                                       float *out, float *red, const Guard &g) {
   bool ok = s.flags[0] == 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;
   const uint8_t *const ring = s.ring;
   uint64_t *const full = s.full, *const empty = s.empty;
   volatile int *const flags = s.flags;
@@ -518,19 +586,22 @@ static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingP
   const int kfull = K / FP8_TILE_COLS * FP8_TILE_COLS;
   for (int g0 = 0; g0 < R; g0 += TILE_ROWS) {
     const int rows = min(TILE_ROWS, R - g0);
-    const int nj = min(ROWS_PER_WARP, (rows - warp + NCW - 1) / NCW);
-    float acc[ROWS_PER_WARP];
-#pragma unroll
-    for (int j = 0; j < ROWS_PER_WARP; ++j) acc[j] = 0.f;
-    switch (nj) {
-      case 4: tile_loop_fp8<4>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
-      case 3: tile_loop_fp8<3>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
-      case 2: tile_loop_fp8<2>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
-      case 1: tile_loop_fp8<1>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
-      default: tile_loop_fp8<0>(ring, full, empty, vec, acc, nslot, slot, phase, kfull, ok, flags, g); break;
+    const int nmb = rows > 16 ? 2 : 1;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (nmb == 2)
+      tile_loop_fp8_mma<2>(ring, full, empty, xh, xl, acc, nslot, slot, phase, kfull, ok, flags, g);
+    else
+      tile_loop_fp8_mma<1>(ring, full, empty, xh, xl, acc, nslot, slot, phase, kfull, ok, flags, g);
+    // column 0 of D is W x_hi, column 1 W x_lo: lane t = 0 of each quad holds both for rows g and g + 8
+    if (ft == 0) {
+      const int r = (nmb == 2 ? 16 * (warp & 1) : 0) + fg;
+      red[warp * TILE_ROWS + r] = acc[0] + acc[1];
+      red[warp * TILE_ROWS + r + 8] = acc[2] + acc[3];
     }
-    if (kfull < K) {  // the last, narrower column block (w codes per row, a multiple of 16)
+    const bool ragged = kfull < K;
+    if (ragged) {  // the last, narrower column block (w codes per row, a multiple of 16): CUDA cores
       const int w = K - kfull;
+      const int nj = min(ROWS_PER_WARP, (rows - warp + NCW - 1) / NCW);
       if (ok && !wait_mbar(&full[slot], phase, g)) {
         ok = false;
         flags[0] = 1;
@@ -549,21 +620,31 @@ static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingP
         slot = 0;
         phase ^= 1u;
       }
+      float tacc[ROWS_PER_WARP] = {0.f, 0.f, 0.f, 0.f};
       if (active) {
-        const float4 *xv = reinterpret_cast<const float4 *>(vec + kfull + lane * 16);
-        const float4 x0 = xv[0], x1 = xv[1], x2 = xv[2], x3 = xv[3];
+        float4 x[4];
+        load_split16(xh + kfull + lane * 16, xl + kfull + lane * 16, x);
 #pragma unroll
         for (int j = 0; j < ROWS_PER_WARP; ++j)
-          if (j < nj) acc[j] += dot16_e4m3(wv[j], x0, x1, x2, x3);
+          if (j < nj) tacc[j] = dot16_e4m3(wv[j], x[0], x[1], x[2], x[3]);
       }
-    }
 #pragma unroll
-    for (int j = 0; j < ROWS_PER_WARP; ++j) {
-      if (j < nj) {
-        const float v = warp_sum(acc[j]);
-        if (lane == 0) out[g0 + warp + NCW * j] = v * scale;
+      for (int j = 0; j < ROWS_PER_WARP; ++j) {
+        if (j < nj) {
+          const float v = warp_sum(tacc[j]);
+          if (lane == 0) red[NCW * TILE_ROWS + warp + NCW * j] = v;
+        }
       }
     }
+    consumer_sync();
+    for (int r = tid; r < rows; r += NCT) {
+      float v = 0.f;
+      for (int w = 0; w < NCW; ++w)
+        if (nmb == 1 || (w & 1) == (r >> 4)) v += red[w * TILE_ROWS + r];
+      if (ragged) v += red[NCW * TILE_ROWS + r];
+      out[g0 + r] = v * scale;
+    }
+    consumer_sync();  // red is reused by the next row group
   }
   rp.slot = slot;
   rp.phase = phase;
@@ -601,15 +682,33 @@ __device__ inline float stage_f32(Smem &s, const float *src, int K, bool want_ss
   return t;
 }
 
+// Four fp32 values as their fp16 high parts hi = fp16(v) (to hi[0..4)) and the fp16 roundings of the
+// remainders v - hi (to lo[0..4)): the two-column B operand of the tensor-core FP8 GEMV.
+__device__ __forceinline__ void split4(const float4 v, __half *hi, __half *lo) {
+  const __half2 h0 = __floats2half2_rn(v.x, v.y), h1 = __floats2half2_rn(v.z, v.w);
+  const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+  const __half2 l0 = __floats2half2_rn(v.x - f0.x, v.y - f0.y), l1 = __floats2half2_rn(v.z - f1.x, v.w - f1.y);
+  uint2 hw, lw;
+  hw.x = *reinterpret_cast<const uint32_t *>(&h0);
+  hw.y = *reinterpret_cast<const uint32_t *>(&h1);
+  lw.x = *reinterpret_cast<const uint32_t *>(&l0);
+  lw.y = *reinterpret_cast<const uint32_t *>(&l1);
+  *reinterpret_cast<uint2 *>(hi) = hw;
+  *reinterpret_cast<uint2 *>(lo) = lw;
+}
+
 // vec[0..K) = src * gain (src fp32 written by other CTAs, read through L2; gain read-only) and the CTA-uniform
 // sum of squares of src (the RMSNorm of src with its gain applied to the staged copy). K a multiple of 4.
-__device__ inline float stage_f32_gain(Smem &s, const float *src, const float *gain, int K) {
+// With `split` the staged values are also written as fp16 high parts split[0..K) and low parts split[K..2K).
+__device__ inline float stage_f32_gain(Smem &s, const float *src, const float *gain, int K, __half *split) {
   const int tid = threadIdx.x;
   float ss = 0.f;
   for (int i = tid * 4; i < K; i += NCT * 4) {
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(src + i));
     const float4 w = __ldg(reinterpret_cast<const float4 *>(gain + i));
-    *reinterpret_cast<float4 *>(s.vec + i) = make_float4(v.x * w.x, v.y * w.y, v.z * w.z, v.w * w.w);
+    const float4 u = make_float4(v.x * w.x, v.y * w.y, v.z * w.z, v.w * w.w);
+    *reinterpret_cast<float4 *>(s.vec + i) = u;
+    if (split) split4(u, split + i, split + K + i);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = warp_sum(ss);
@@ -620,6 +719,14 @@ __device__ inline float stage_f32_gain(Smem &s, const float *src, const float *g
   for (int w = 0; w < NCW; ++w) t += s.red[w];
   consumer_sync();
   return t;
+}
+
+// split[0..K) = fp16 high parts and split[K..2K) = fp16 low parts of src (fp32 written by other CTAs, read
+// through L2); nothing else is staged. K a multiple of 4.
+__device__ inline void stage_split(const float *src, int K, __half *split) {
+  for (int i = threadIdx.x * 4; i < K; i += NCT * 4)
+    split4(__ldcg(reinterpret_cast<const float4 *>(src + i)), split + i, split + K + i);
+  consumer_sync();
 }
 
 // vec[0..K) = fp32(src) for an fp16 vector that is read-only during the launch.

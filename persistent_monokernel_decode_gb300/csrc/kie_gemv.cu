@@ -65,7 +65,8 @@ __global__ void pack_kernel(const uint16_t *src, uint16_t *dst, int M, int K, in
   }
 }
 
-// dst = packed(src) for FP8 codes [M, K] (column blocks of FP8_TILE_COLS codes). With b == null row r is
+// dst = packed(src) for FP8 codes [M, K] (packed_offset_fp8: column blocks of FP8_TILE_COLS codes, chunks of
+// odd rows swizzled in full blocks). With b == null row r is
 // a[r]; otherwise rows interleave two [M/2, K] matrices: row 2i = a[i], row 2i + 1 = b[i] (gate/up pairs).
 // One thread moves 16 consecutive codes of one row; K is a multiple of 16.
 __global__ void pack_fp8_kernel(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n) {
@@ -75,8 +76,7 @@ __global__ void pack_fp8_kernel(const uint8_t *a, const uint8_t *b, uint8_t *dst
     const int r = (int)(idx / (K / 16));
     const int c = (int)(idx % (K / 16)) * 16;
     const uint8_t *src = b ? ((r & 1) ? b : a) + (size_t)(r >> 1) * K + c : a + (size_t)r * K + c;
-    *reinterpret_cast<uint4 *>(dst + packed_offset_bw(M, K, n, r, c, FP8_TILE_COLS)) =
-        *reinterpret_cast<const uint4 *>(src);
+    *reinterpret_cast<uint4 *>(dst + packed_offset_fp8(M, K, n, r, c)) = *reinterpret_cast<const uint4 *>(src);
   }
 }
 

@@ -59,4 +59,17 @@ KIE_HD long long packed_offset_bw(int M, int K, int n, int r, int c, int bw) {
 // Element offset of W[r][c] in a packed fp16 matrix (column blocks of TILE_COLS).
 KIE_HD long long packed_offset(int M, int K, int n, int r, int c) { return packed_offset_bw(M, K, n, r, c, TILE_COLS); }
 
+// Byte offset of code Q[r][c] in a packed FP8 matrix: column blocks of FP8_TILE_COLS codes; within a full block
+// the 16-code chunk q of row r sits at chunk q ^ 4 when r is odd (row-major otherwise). Rows are split over
+// CTAs in pairs, so a row's parity is also its parity within its tile, and within two tiles of the same rows
+// copied back to back. The swizzle lets the tensor-core consumer's lanes of two neighbouring rows read the
+// same chunk columns from different halves of a 128-byte line (no shared-memory bank conflict).
+KIE_HD long long packed_offset_fp8(int M, int K, int n, int r, int c) {
+  const long long o = packed_offset_bw(M, K, n, r, c, FP8_TILE_COLS);
+  const int b = c / FP8_TILE_COLS;
+  if (K - b * FP8_TILE_COLS < FP8_TILE_COLS || !(r & 1)) return o;
+  const int q = (c - b * FP8_TILE_COLS) >> 4;
+  return o + (long long)(((q ^ 4) - q) * 16);
+}
+
 }  // namespace kie

@@ -57,9 +57,20 @@ def test_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
 @pytest.mark.parametrize("M,K,n", [(2, 16, 1), (256, 256, 152), (256, 128, 152), (34, 784, 3), (66, 528, 5),
                                    (100, 1040, 7), (2048, 1024, 152)])
 def test_fp8_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
-    """FP8 expert matrices: one-byte codes in 512-code column blocks, so a full 32-row tile is again 16 KB."""
+    """FP8 expert matrices: one-byte codes in 512-code column blocks, so a full 32-row tile is again 16 KB. Each
+    tile is one contiguous run of its rows; in a full 512-code block the 16-code chunk q of an odd row sits at
+    chunk q ^ 4 of the row, elsewhere rows are plain row-major."""
     off = np.array([[kie.packed_offset_fp8(M, K, n, r, c) for c in range(K)] for r in range(M)], dtype=np.int64)
     assert np.array_equal(np.sort(off.ravel()), np.arange(M * K))
+    for r in range(M):
+        for k0 in range(0, K, 512):
+            w = min(512, K - k0)
+            row = off[r, k0:k0 + w]
+            base = row.min()
+            assert row.max() == base + w - 1  # a row of a tile is one run of w bytes
+            c = np.arange(w)
+            want = c if (w < 512 or r % 2 == 0) else ((c // 16) ^ 4) * 16 + c % 16
+            assert np.array_equal(row - base, want), (r, k0)
     for cta in range(n):
         r0, r1 = kie.rows_of_cta(M, n, cta)
         if r1 == r0:
@@ -71,7 +82,8 @@ def test_fp8_packed_layout_is_a_bijection_with_contiguous_tiles(M, K, n):
             for k0 in range(0, K, 512):
                 w = min(512, K - k0)
                 tile = block[g0:g0 + rows, k0:k0 + w]
-                assert np.array_equal(tile.ravel() - tile.min(), np.arange(rows * w))
+                assert np.array_equal(np.sort(tile.ravel()) - tile.min(), np.arange(rows * w))
+                assert np.array_equal(tile.min(axis=1) - tile.min(), np.arange(rows) * w)  # rows in order
                 assert tile.min() % 16 == 0 and (rows * w) % 16 == 0  # a legal bulk copy
     assert kie.packed_offset_fp8(M, K + 8, n, 0, 0) == -1  # K must be a multiple of 16
 
