@@ -148,14 +148,15 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   __half *qA = reinterpret_cast<__half *>(s.vec);    // [16][RS] q / sqrt(dh): high parts, low parts
   __half *Ks = qA + 16 * RS;                         // [ATT_SUB][RS]
   __half *Vs = Ks + ATT_SUB * RS;                    // [ATT_SUB][RS]
-  float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * RS);  // [MAX_GROUP][ATT_SUB] scores
+  float *ps = reinterpret_cast<float *>(Vs + ATT_SUB * RS);  // [MAX_GROUP][ATT_SUB] softmax scratch:
+  float *pmax = ps, *psum = ps + 4 * 8, *mnew = ps + 8 * 8;  // [4 warps][8 heads] partial maxima and sums
   __half *PA = reinterpret_cast<__half *>(ps + MAX_GROUP * ATT_SUB);  // [16][PS] p: high parts, low parts
   float *corr = reinterpret_cast<float *>(PA + 16 * PS);  // [MAX_GROUP]
   float *mrun = corr + MAX_GROUP;
   float *lrun = mrun + MAX_GROUP;
   float *mw = lrun + MAX_GROUP;                        // merge: [smax][G] m, then weights
   float *ml = mw + p.smax * G;                         // merge: [smax][G] l
-  const float scale = 1.0f / sqrtf((float)DH);
+  const float scale = 1.4426950408889634f / sqrtf((float)DH);  // log2(e) / sqrt(dh): scores in log2 units
   const size_t plane = (size_t)p.max_seq * DH;
   const __half *Kb = p.kv + ((size_t)l * 2 * p.Hkv + kh) * plane;
   const __half *Vb = p.kv + ((size_t)l * 2 * p.Hkv + p.Hkv + kh) * plane;
@@ -220,36 +221,53 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     stash(jb);
     consumer_sync();                               // Ks, Vs (and qA, PA) ready; ps free
     if (jb + ATT_SUB < j1) fetch(jb + ATT_SUB);    // next sub-chunk in flight while this one is used
-    // scores: warp w < 4 takes positions [8w, 8w + 8) of the sub-chunk over DH / 16 steps of 16
+    // scores S = Q K^T in log2 units: warp w < 4 takes positions [8w, 8w + 8) of the sub-chunk (two accumulator
+    // chains over the DH / 16 steps of 16). Lane (g, t) holds head g's scores at positions 8w + 2t, 8w + 2t + 1
+    // (rows g and 8 + g of D, the q high and low parts, summed); positions past nb weigh 0. The warp's maximum
+    // per head comes from the lane's quad (two shuffles), and the four warps' maxima meet in shared memory.
+    float s0 = -INFINITY, s1 = -INFINITY;
     if (warp < ATT_SUB / 8) {
-      const int n0 = warp * 8;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const int n0 = warp * 8, p0 = n0 + 2 * ft;
+      float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
       for (int ks = 0; ks < DH / 16; ++ks) {
         uint32_t a[4], b[2];
         ldsm_x4(a, qA + arow * RS + ks * 16 + acol);
         ldsm_x2(b, Ks + (n0 + (lane & 7)) * RS + ks * 16 + 8 * ((lane >> 3) & 1));
-        mma_f16_f32(c, a, b);
+        mma_f16_f32(c[ks & 1], a, b);
       }
-      if (fg < G)
-        *reinterpret_cast<float2 *>(ps + fg * ATT_SUB + n0 + 2 * ft) = make_float2(c[0] + c[2], c[1] + c[3]);
+      if (p0 < nb) s0 = (c[0][0] + c[0][2]) + (c[1][0] + c[1][2]);
+      if (p0 + 1 < nb) s1 = (c[0][1] + c[0][3]) + (c[1][1] + c[1][3]);
+      float m8 = fmaxf(s0, s1);
+      m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 1));
+      m8 = fmaxf(m8, __shfl_xor_sync(0xffffffffu, m8, 2));
+      if (ft == 0) pmax[warp * 8 + fg] = m8;
     }
     consumer_sync();
-    // online-softmax update: warp h owns query head h, lane j position jb + j; positions past nb weigh 0
-    if (warp < G) {
-      const int h = warp, jj = lane;
-      const float sc = jj < nb ? ps[h * ATT_SUB + jj] : -INFINITY;
-      const float mnew = fmaxf(mrun[h], warp_max(sc));
-      const float e = jj < nb ? expf(sc - mnew) : 0.f;
-      const __half hi = __float2half_rn(e);
-      PA[h * PS + jj] = hi;
-      PA[(8 + h) * PS + jj] = __float2half_rn(e - __half2float(hi));
-      const float sum = warp_sum(e);
-      if (lane == 0) {
-        const float cr = expf(mrun[h] - mnew);
-        corr[h] = cr;
-        lrun[h] = lrun[h] * cr + sum;
-        mrun[h] = mnew;
+    // online softmax, in the same lanes: m_new = max(m_run, the four warps' maxima), p = 2^(s - m_new) into rows
+    // h (fp16 high part) and 8 + h (fp16 remainder) of the P operand, the warp's partial sums per head; warp 0
+    // also leaves m_new and the rescale factor 2^(m_run - m_new) for the P V step. Lanes of heads past the group
+    // compute on zero rows and store nothing.
+    if (warp < ATT_SUB / 8) {
+      const int p0 = warp * 8 + 2 * ft;
+      const float mo = mrun[fg];
+      const float mn = fmaxf(fmaxf(mo, fmaxf(pmax[fg], pmax[8 + fg])), fmaxf(pmax[16 + fg], pmax[24 + fg]));
+      const float e0 = exp2f(s0 - mn), e1 = exp2f(s1 - mn);
+      float sm = e0 + e1;
+      sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+      sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+      if (fg < G) {
+        const __half2 hi = __floats2half2_rn(e0, e1);
+        const float2 hf = __half22float2(hi);
+        *reinterpret_cast<__half2 *>(PA + fg * PS + p0) = hi;
+        *reinterpret_cast<__half2 *>(PA + (8 + fg) * PS + p0) = __floats2half2_rn(e0 - hf.x, e1 - hf.y);
+        if (ft == 0) {
+          psum[warp * 8 + fg] = sm;
+          if (warp == 0) {
+            mnew[fg] = mn;
+            corr[fg] = exp2f(mo - mn);
+          }
+        }
       }
     }
     consumer_sync();
@@ -273,7 +291,11 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
         }
       }
     }
-    consumer_sync();                               // Ks, Vs, ps, PA reused by the next sub-chunk
+    if (tid < G) {  // the running sum and maximum of head tid (every reader of the old values is past)
+      lrun[tid] = lrun[tid] * corr[tid] + ((psum[tid] + psum[8 + tid]) + (psum[16 + tid] + psum[24 + tid]));
+      mrun[tid] = mnew[tid];
+    }
+    consumer_sync();                               // Ks, Vs, PA and the softmax scratch reused next
   }
 
   // publish (m, l, o) of this piece
@@ -316,7 +338,8 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
   if (s.flags[0]) return;
 
   // Merge, split across the S pieces of the head: this CTA produces outputs [e0, e1) of the E,
-  //   o_e = sum_q w_q o_q,e   with   w_q = exp(m_q - M) / sum_r exp(m_r - M) l_r,   M = max_r m_r
+  //   o_e = sum_q w_q o_q,e   with   w_q = 2^(m_q - M) / sum_r 2^(m_r - M) l_r,   M = max_r m_r
+  // (the maxima m are in log2 units, like the scores)
   // for the query head of e. Every value it needs (all (m, l) of the head, and its slice of every piece's o)
   // is requested before any is used: one round trip.
   const int sl = (E + S - 1) / S;
@@ -352,13 +375,22 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     for (int q = lane; q < S; q += 32) mx = fmaxf(mx, mw[q * G + h]);
     mx = warp_max(mx);
     float den = 0.f;
-    for (int q = lane; q < S; q += 32) den = fmaf(expf(mw[q * G + h] - mx), ml[q * G + h], den);
+    for (int q = lane; q < S; q += 32) den = fmaf(exp2f(mw[q * G + h] - mx), ml[q * G + h], den);
     den = warp_sum(den);
     const float inv = 1.0f / den;
-    for (int q = lane; q < S; q += 32) mw[q * G + h] = expf(mw[q * G + h] - mx) * inv;
+    for (int q = lane; q < S; q += 32) mw[q * G + h] = exp2f(mw[q * G + h] - mx) * inv;
   }
   consumer_sync();
-  // P threads per output, each over every P-th piece, then a sum over the P partials
+  if (S <= 16) {  // few pieces: one thread per output, over all pieces in order
+    for (int i = tid; i < w; i += NCT) {
+      const int h = (e0 + i) / DH;
+      float a = 0.f;
+      for (int q = 0; q < S; ++q) a = fmaf(mw[q * G + h], mo[q * w + i], a);
+      p.o[(size_t)kh * E + e0 + i] = a;
+    }
+    return;
+  }
+  // many pieces: P threads per output, each over every P-th piece, then a sum over the P partials
   float *red = reinterpret_cast<float *>(Vs);  // [P][w]; mo ends before the V half of the staging area
   const int P = max(1, NCT / w);
   for (int idx = tid; idx < P * w; idx += NCT) {
