@@ -369,6 +369,22 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     }
   }
   consumer_sync();
+  if (S <= 16) {  // few pieces: each output's thread takes its head's maximum and normaliser itself (no
+                  // cross-lane reduction, no further barrier), then sums the pieces in order
+    for (int i = tid; i < w; i += NCT) {
+      const int h = (e0 + i) / DH;
+      float mx = -INFINITY;
+      for (int q = 0; q < S; ++q) mx = fmaxf(mx, mw[q * G + h]);
+      float den = 0.f, a = 0.f;
+      for (int q = 0; q < S; ++q) {
+        const float wq = exp2f(mw[q * G + h] - mx);
+        den = fmaf(wq, ml[q * G + h], den);
+        a = fmaf(wq, mo[q * w + i], a);
+      }
+      p.o[(size_t)kh * E + e0 + i] = a / den;
+    }
+    return;
+  }
   if (warp < G) {  // warp h: the weights of query head h, lane per piece
     const int h = warp;
     float mx = -INFINITY;
@@ -381,15 +397,6 @@ __device__ inline void attention_piece(const DecodeParams &p, Smem &s, int l, in
     for (int q = lane; q < S; q += 32) mw[q * G + h] = exp2f(mw[q * G + h] - mx) * inv;
   }
   consumer_sync();
-  if (S <= 16) {  // few pieces: one thread per output, over all pieces in order
-    for (int i = tid; i < w; i += NCT) {
-      const int h = (e0 + i) / DH;
-      float a = 0.f;
-      for (int q = 0; q < S; ++q) a = fmaf(mw[q * G + h], mo[q * w + i], a);
-      p.o[(size_t)kh * E + e0 + i] = a;
-    }
-    return;
-  }
   // many pieces: P threads per output, each over every P-th piece, then a sum over the P partials
   float *red = reinterpret_cast<float *>(Vs);  // [P][w]; mo ends before the V half of the staging area
   const int P = max(1, NCT / w);
