@@ -233,7 +233,7 @@ int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
  * being code value * row scale. out = sum over the routed experts j of w_j * Wd_j (silu(Wg_j u) * (Wu_j u)).
  * Attention, norms, embedding and LM head are those of the dense model. Decode runs the same monokernel with
  * the router, the top_k selection and the two expert projections as grid phases: after the router the
- * producer warp streams only the routed experts' FP8 tiles.
+ * producer streams only the routed experts' FP8 tiles.
  *
  * Requirements: 1 <= n_experts <= 256, 1 <= top_k <= min(8, n_experts), d_model and ffn_dim multiples of 16.
  * Prefill of a MoE ctx runs the prompt through the decode kernel one position after another (teacher forcing,

@@ -763,21 +763,27 @@ __global__ void __launch_bounds__(BLOCK, 1) decode_kernel(const DecodeParams p) 
   init_ring(s, p.nslot);
   const Guard g{&p.ctl->status, p.timeout_ns};
   if (threadIdx.x >= NCT) {
+    regs_release<PRODUCER_REGS>();
     if (threadIdx.x == NCT) producer_main(p, s, g, MOE);
     return;
   }
+  regs_acquire<CONSUMER_REGS>();
   consumer_main<MOE>(p, s, g);
 }
 
 // The split-KV attention step alone (profiling): layers [0, n_layers) over c cached positions, with whatever q and
-// cache the workspace holds, through the same device function and grid barrier as decode_kernel. The producer
-// warp has nothing to stream and leaves after the ring set-up.
+// cache the workspace holds, through the same device function, register split and grid barrier as decode_kernel.
+// The producer warpgroup has nothing to stream and leaves after the ring set-up.
 __global__ void __launch_bounds__(BLOCK, 1) attention_kernel(const DecodeParams p, int c, int n_layers) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem s = carve_smem(smem_raw, p.nslot, p.vec_floats, p.out_floats);
   init_ring(s, p.nslot);
   const Guard g{&p.ctl->status, p.timeout_ns};
-  if (threadIdx.x >= NCT) return;
+  if (threadIdx.x >= NCT) {
+    regs_release<PRODUCER_REGS>();
+    return;
+  }
+  regs_acquire<CONSUMER_REGS>();
   uint32_t gen = 0;
   unsigned att_target = 0;
   unsigned long long wait_ns = 0;
@@ -806,9 +812,20 @@ __global__ void __launch_bounds__(BLOCK, 1) attention_kernel(const DecodeParams 
 
 }  // namespace kie
 
+// The register split inside the kernel is sized for LAUNCH_REGS per thread at launch; a build that compiled the
+// kernel to fewer would leave the consumers' register increase waiting forever, so it is never launched.
+static cudaError_t check_register_split(const void *fn) {
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, fn);
+  if (e != cudaSuccess) return e;
+  return a.numRegs >= kie::LAUNCH_REGS ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 cudaError_t kie_launch_attention(const kie::DecodeParams &p, size_t smem, int c, int n_layers, cudaStream_t stream) {
   const void *fn = (const void *)kie::attention_kernel;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = check_register_split(fn);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&p, (void *)&c, (void *)&n_layers};
   return cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kie::BLOCK), args, smem, stream);
@@ -817,7 +834,9 @@ cudaError_t kie_launch_attention(const kie::DecodeParams &p, size_t smem, int c,
 // Launch helper used by the C ABI (kie_api.cu).
 cudaError_t kie_launch_decode(const kie::DecodeParams &p, size_t smem, cudaStream_t stream) {
   const void *fn = p.E > 0 ? (const void *)kie::decode_kernel<true> : (const void *)kie::decode_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = check_register_split(fn);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {(void *)&p};
   return cudaLaunchCooperativeKernel(fn, dim3(p.n_cta), dim3(kie::BLOCK), args, smem, stream);

@@ -1,6 +1,7 @@
 // Device building blocks shared by the persistent decode kernel and the standalone GEMV kernel.
 //
-// Every CTA runs NCW consumer warps and one producer warp. The producer's elected lane walks the CTA's
+// Every CTA runs NCW consumer warps and one producer warpgroup, whose first lane is the producer and whose
+// registers mostly go to the consumers (setmaxnreg). The producer walks the CTA's
 // static sequence of weight tiles (it does not depend on any activation) and moves each tile from HBM
 // into a shared-memory ring slot with one 1-D bulk copy (cp.async.bulk, completion counted on the slot's
 // "full" mbarrier, L2 evict-first policy). Consumers wait on "full", run their part of the dot products
@@ -20,7 +21,15 @@ namespace kie {
 
 constexpr int NCW = 8;                          // consumer warps
 constexpr int NCT = NCW * 32;                   // consumer threads
-constexpr int BLOCK = NCT + 32;                 // + one producer warp
+constexpr int BLOCK = NCT + 128;                // + one producer warpgroup (one lane streams the weights)
+// Register split of the decode kernel (setmaxnreg): the block launches with LAUNCH_REGS per thread, the producer
+// warpgroup drops to PRODUCER_REGS and hands the rest to the two consumer warpgroups, which rise to
+// CONSUMER_REGS. The counts must balance exactly against the launch, or the consumers' increase would wait for
+// registers that never come: the launch path checks the compiled count before every launch.
+constexpr int LAUNCH_REGS = 168, PRODUCER_REGS = 40, CONSUMER_REGS = 232;
+static_assert(NCT * CONSUMER_REGS + (BLOCK - NCT) * PRODUCER_REGS <= BLOCK * LAUNCH_REGS,
+              "the register split must fit in the launch allocation");
+static_assert(BLOCK * LAUNCH_REGS <= 65536, "one block per SM");
 constexpr int ROWS_PER_WARP = TILE_ROWS / NCW;  // rows of a tile each consumer warp owns
 constexpr int FP8_RED_FLOATS = (NCW + 1) * TILE_ROWS;  // partial sums of one FP8 row group
 static_assert(TILE_ROWS % NCW == 0, "tile rows must split evenly over consumer warps");
@@ -107,7 +116,17 @@ __device__ __forceinline__ int ld_relaxed_gpu(const int *p) {
   return v;
 }
 
-// Named barrier 1: the NCT consumer threads of this CTA (the producer warp never joins it).
+// Register reallocation between warpgroups (all threads of a warpgroup execute the same one).
+template <int N>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_acquire() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+
+// Named barrier 1: the NCT consumer threads of this CTA (the producer warpgroup never joins it).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -210,7 +229,7 @@ __device__ inline Smem carve_smem(uint8_t *base, int nslot, int vec_floats, int 
   return s;
 }
 
-// Thread 0 initialises the ring barriers; every thread of the block (producer warp included) must call.
+// Thread 0 initialises the ring barriers; every thread of the block (producer warpgroup included) must call.
 __device__ inline void init_ring(Smem &s, int nslot) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < nslot; ++i) {
