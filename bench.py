@@ -55,9 +55,10 @@ def phase_bytes(model, c):
 
 
 def phase_names(model):
-    """The grid phases of one layer, in order."""
+    """The grid phases of one layer, in order (sparse MoE: the router is folded into the QKV and WO phases, and the
+    expert gate/up phase starts with the selection)."""
     if getattr(model, "n_experts", 0):
-        return ["qkv", "att", "wo", "router", "egu", "edown"]
+        return ["qkv", "att", "wo", "egu", "edown"]
     return ["qkv", "att", "wo", "gu", "down"]
 
 

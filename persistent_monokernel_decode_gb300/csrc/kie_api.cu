@@ -22,6 +22,8 @@ cudaError_t kie_launch_gemv(const uint8_t *packed, const __half *x, float *y, in
                             unsigned long long timeout_ns, cudaStream_t stream);
 cudaError_t kie_launch_pack(const uint16_t *src, uint16_t *dst, int M, int K, int n_cta, const uint16_t *gain,
                             cudaStream_t stream);
+cudaError_t kie_launch_fold_router(const float *rg, const uint16_t *wo, float *out, int E, int d, int dq,
+                                   cudaStream_t stream);
 cudaError_t kie_launch_pack_fp8(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n_cta,
                                 cudaStream_t stream);
 
@@ -36,12 +38,13 @@ thread_local std::string g_create_error;
 size_t al(size_t v) { return kie::align_up(v, ALIGN); }
 
 // Byte offsets of the device weight buffer. Per layer (layer_stride apart): qkv, wo, then the dense FFN (gu,
-// down) or the sparse-MoE FFN (router, egu/edn: n_experts packed FP8 matrices egu_bytes/edn_bytes apart,
-// esgu/esdn: their row scales). Then the LM head, the embedding and (MoE) the fp32 FFN gains [L][d].
+// down) or the sparse-MoE FFN (the router folded by linearity: rg = router o g_ffn [E][d] and rgwo = rg Wo
+// [E][dq], both fp32; egu/edn: n_experts packed FP8 matrices egu_bytes/edn_bytes apart, esgu/esdn: their row
+// scales). Then the LM head, the embedding and (MoE) the fp32 FFN gains [L][d].
 // Dense models also keep each layer's four projections as canonical tensor-core tiles for the batched prefill
 // (tc, tc_layer_stride apart, tc_off[QKV, WO, GU, DOWN] within a layer).
 struct WeightLayout {
-  size_t qkv, wo, gu, down, router, egu, edn, esgu, esdn, egu_bytes, edn_bytes, layer_stride, lm, embed, gffn, tc,
+  size_t qkv, wo, gu, down, rg, rgwo, egu, edn, esgu, esdn, egu_bytes, edn_bytes, layer_stride, lm, embed, gffn, tc,
       tc_layer_stride, tc_off[4], total;
 };
 
@@ -87,7 +90,7 @@ ScratchLayout scratch_layout(const kie_config *c, const kie_moe_config *moe, int
   s.q = take((size_t)dq * 4);
   s.o = take((size_t)dq * 4);
   s.a = take((size_t)c->ffn_dim * std::max(1, topk) * 4);
-  s.rlog = take((size_t)E * 4);
+  s.rlog = take((size_t)2 * E * 4);  // the two partial router logits (from x and from o) of each expert
   s.part_o = take((size_t)c->n_kv_heads * smax * G * c->head_dim * 4);
   s.part_ml = take((size_t)c->n_kv_heads * smax * G * 2 * 4);
   s.ctl = take(sizeof(kie::Ctl));
@@ -163,8 +166,9 @@ const char *make_plan(const kie_config *c, const kie_moe_config *moe, int n_cta,
     w.down = w.gu + al((size_t)2 * F * d * 2);
     w.layer_stride = w.down + al((size_t)d * F * 2);
   } else {
-    w.router = w.wo + al((size_t)d * dq * 2);
-    w.egu = w.router + al((size_t)E * d * 2);
+    w.rg = w.wo + al((size_t)d * dq * 2);
+    w.rgwo = w.rg + al((size_t)E * d * 4);
+    w.egu = w.rgwo + al((size_t)E * dq * 4);
     w.egu_bytes = al((size_t)2 * F * d);
     w.edn = w.egu + E * w.egu_bytes;
     w.edn_bytes = al((size_t)d * F);
@@ -338,14 +342,31 @@ int upload(kie_ctx *ctx, uint8_t *dst, const void *host, size_t bytes) {
   return KIE_OK;
 }
 
-// The sparse-MoE FFN of layer l: router as given, each expert's FP8 gate/up (rows interleaved) and down matrices
-// packed through `stage` (>= 2 * F * d bytes), row scales interleaved like the rows, FFN gain as fp32.
+// The sparse-MoE FFN of layer l: the router folded by linearity (rg = router o g_ffn, exact in fp32, and
+// rgwo = rg Wo in fp64 on the device, rounded to fp32), each expert's FP8 gate/up (rows interleaved) and down
+// matrices packed through `stage` (>= 2 * max(F, dq) * d bytes), row scales interleaved like the rows, FFN gain
+// as fp32.
 int repack_moe_layer(kie_ctx *ctx, const kie_weights *w, const kie_moe_weights *mw, int l, uint8_t *stage) {
   const kie_config &c = ctx->cfg;
   const Plan &pl = ctx->plan;
-  const int d = c.d_model, F = c.ffn_dim, E = ctx->moe.n_experts;
+  const int d = c.d_model, F = c.ffn_dim, E = ctx->moe.n_experts, dq = c.n_heads * c.head_dim;
   uint8_t *lw = ctx->wbuf + (size_t)l * pl.w.layer_stride;
-  int rc = upload(ctx, lw + pl.w.router, mw->router[l], (size_t)E * d * 2);
+  std::vector<float> rg((size_t)E * d);
+  for (int e = 0; e < E; ++e)
+    for (int j = 0; j < d; ++j) {
+      __half_raw r, g;
+      r.x = mw->router[l][(size_t)e * d + j];
+      g.x = w->ffn_norm[l][j];
+      rg[(size_t)e * d + j] = __half2float(__half(r)) * __half2float(__half(g));  // exact: 11 x 11 bits
+    }
+  int rc = upload(ctx, lw + pl.w.rg, rg.data(), rg.size() * 4);
+  if (rc == KIE_OK) rc = upload(ctx, stage, w->wo[l], (size_t)d * dq * 2);
+  if (rc == KIE_OK) {
+    KIE_CUDA(ctx, kie_launch_fold_router(reinterpret_cast<const float *>(lw + pl.w.rg),
+                                         reinterpret_cast<const uint16_t *>(stage),
+                                         reinterpret_cast<float *>(lw + pl.w.rgwo), E, d, dq, ctx->stream));
+    KIE_CUDA(ctx, cudaStreamSynchronize(ctx->stream));  // rg (host) and the staged Wo are reused below
+  }
   for (int e = 0; e < E && rc == KIE_OK; ++e) {
     const size_t m = (size_t)F * d;
     rc = upload(ctx, stage, mw->gate_q[l] + (size_t)e * m, m);
@@ -481,7 +502,8 @@ void fill_base(kie_ctx *ctx) {
   p.out_moe = pl.out_moe;
   p.E = ctx->moe.n_experts;
   p.top_k = ctx->moe.top_k;
-  p.off_router = (long long)pl.w.router;
+  p.off_rg = (long long)pl.w.rg;
+  p.off_rgwo = (long long)pl.w.rgwo;
   p.off_egu = (long long)pl.w.egu;
   p.off_edn = (long long)pl.w.edn;
   p.off_esgu = (long long)pl.w.esgu;

@@ -439,36 +439,81 @@ __device__ __forceinline__ MoeSel moe_sel(const DecodeParams &p, const Smem &s) 
   return {reinterpret_cast<uint64_t *>(b), reinterpret_cast<int *>(b + 2), b + 2 + MAX_TOP_K};
 }
 
-// Router logits of u = inv_rms(h) * (g o h) for this CTA's router rows (e = CTA, CTA + n_cta, ...): the staged
-// vector already holds g o h, `inv` is inv_rms(h). Rows are read straight from global memory (prefetched into L2
-// at the start of the layer); a CTA-wide dot product per row, summed in a fixed order.
-__device__ inline void moe_router(const DecodeParams &p, Smem &s, int l, float inv) {
+// The router by linearity. Its logits are inv_rms(h) * (R (g o h)) with h = x + Wo o, so with rg = R diag(g)
+// and rgwo = rg Wo (folded at creation) they are inv_rms(h) * (rg x + rgwo o): rg x is taken in the QKV phase
+// (x is staged there), rgwo o in the WO phase (o is staged there), and the logits need no phase and no grid
+// barrier of their own. This CTA's rows e = CTA, CTA + n_cta, ... of the K-column fp32 matrix M times the staged
+// vector, into out[e]: the first row is requested into registers when the phase starts (RouterRow), so its L2
+// round trip overlaps the phase's GEMV (staging it in shared memory with cp.async instead measured slower); any
+// further rows (more experts than CTAs) are read afterwards. A CTA-wide dot product per row, summed in a fixed
+// order.
+constexpr int ROUTER_V4 = 4;  // float4 per thread held for the first row: rows of up to 4 * 4 * NCT columns
+
+struct RouterRow {
+  float4 v[ROUTER_V4];
+};
+
+__device__ __forceinline__ RouterRow moe_router_fetch(const DecodeParams &p, const float *M, int K) {
+  RouterRow r;
+  const int e = blockIdx.x;
+#pragma unroll
+  for (int i = 0; i < ROUTER_V4; ++i) {
+    const int k = (threadIdx.x + i * NCT) * 4;
+    r.v[i] = (e < p.E && k < K) ? __ldg(reinterpret_cast<const float4 *>(M + (size_t)e * K + k))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  return r;
+}
+
+__device__ inline void moe_router_part(const DecodeParams &p, Smem &s, const RouterRow &first, const float *M, int K,
+                                       float *out) {
   const int tid = threadIdx.x;
-  const __half *R = reinterpret_cast<const __half *>(p.wbase + (size_t)l * p.layer_stride + p.off_router);
   for (int e = blockIdx.x; e < p.E; e += p.n_cta) {
-    float acc = 0.f;
-    for (int k = tid * 8; k < p.d; k += NCT * 8) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(R + (size_t)e * p.d + k));
-      acc += dot8(raw, *reinterpret_cast<const float4 *>(s.vec + k), *reinterpret_cast<const float4 *>(s.vec + k + 4));
+    float a0 = 0.f, a1 = 0.f;
+    if (e == (int)blockIdx.x && K <= ROUTER_V4 * NCT * 4) {
+#pragma unroll
+      for (int i = 0; i < ROUTER_V4; ++i) {
+        const int k = (tid + i * NCT) * 4;
+        if (k < K) {
+          const float4 w = first.v[i], v = *reinterpret_cast<const float4 *>(s.vec + k);
+          a0 = fmaf(w.x, v.x, a0);
+          a1 = fmaf(w.y, v.y, a1);
+          a0 = fmaf(w.z, v.z, a0);
+          a1 = fmaf(w.w, v.w, a1);
+        }
+      }
+    } else {
+      for (int k = tid * 4; k < K; k += NCT * 4) {
+        const float4 w = __ldg(reinterpret_cast<const float4 *>(M + (size_t)e * K + k));
+        const float4 v = *reinterpret_cast<const float4 *>(s.vec + k);
+        a0 = fmaf(w.x, v.x, a0);
+        a1 = fmaf(w.y, v.y, a1);
+        a0 = fmaf(w.z, v.z, a0);
+        a1 = fmaf(w.w, v.w, a1);
+      }
     }
-    acc = warp_sum(acc);
+    const float acc = warp_sum(a0 + a1);
     if ((tid & 31) == 0) s.red[tid >> 5] = acc;
     consumer_sync();
     if (tid == 0) {
       float t = 0.f;
-      for (int w = 0; w < NCW; ++w) t += s.red[w];
-      p.rlog[e] = t * inv;
+      for (int w8 = 0; w8 < NCW; ++w8) t += s.red[w8];
+      out[e] = t;
     }
     consumer_sync();
   }
 }
 
-// Every CTA, after the router barrier: the top_k largest logits (the lowest id first among equal ones), in
-// descending order, and the softmax over them; warp 0 computes it (all CTAs get identical results from identical
-// inputs), publishes it to the producer through the selection mbarrier, and every consumer sees it after the
-// closing consumer_sync. With p.forced_experts the given experts of (token t, layer l) are used instead of the
-// own selection (which still goes to p.out_experts).
-__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel, int t, int l) {
+// Every CTA, after the WO barrier: the router logits inv * (rg x + rgwo o), the top_k largest (the lowest id
+// first among equal ones), in descending order, and the softmax over them; warp 0 computes it (all CTAs get
+// identical results from identical inputs), publishes it to the producer through the selection mbarrier, and every
+// consumer sees it after the closing consumer_sync. With p.forced_experts the given experts of (token t, layer l)
+// are used instead of the own selection (which still goes to p.out_experts).
+__device__ __forceinline__ float moe_logit(const DecodeParams &p, int e, float inv) {
+  return (__ldcg(p.rlog + e) + __ldcg(p.rlog + p.E + e)) * inv;
+}
+
+__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel, int t, int l, float inv) {
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid < 32) {
     constexpr int PER = MAX_EXPERTS / 32;
@@ -476,7 +521,7 @@ __device__ inline void moe_select(const DecodeParams &p, const Smem &s, const Mo
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      key[i] = e < p.E ? argmax_key(__ldcg(p.rlog + e), e) : 0ull;
+      key[i] = e < p.E ? argmax_key(moe_logit(p, e, inv), e) : 0ull;
     }
     int mine = 0;
     for (int j = 0; j < p.top_k; ++j) {
@@ -497,7 +542,7 @@ __device__ inline void moe_select(const DecodeParams &p, const Smem &s, const Mo
     const size_t at = ((size_t)t * p.L + l) * p.top_k + lane;
     if (p.out_experts && blockIdx.x == 0 && lane < p.top_k) p.out_experts[at] = mine;
     if (p.forced_experts && lane < p.top_k) mine = p.forced_experts[at];  // ids checked on the host
-    const float v = lane < p.top_k ? __ldcg(p.rlog + mine) : -INFINITY;
+    const float v = lane < p.top_k ? moe_logit(p, mine, inv) : -INFINITY;
     const float mx = warp_max(v);
     const float ev = lane < p.top_k ? expf(v - mx) : 0.f;
     const float sum = warp_sum(ev);
@@ -604,13 +649,20 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
             bulk_prefetch_l2(Vb, (uint32_t)((j1 - j0) * p.dh * 2));
           }
         }
-        if (MOE && tid == 0)  // this CTA's router rows, read once h is known
-          for (int e = blockIdx.x; e < p.E; e += p.n_cta)
-            bulk_prefetch_l2(p.wbase + (size_t)l * p.layer_stride + p.off_router + (size_t)e * p.d * 2, (uint32_t)p.d * 2);
+        if (MOE && tid == 0)  // this CTA's rows of the folded router, used at the end of the QKV and WO phases
+          for (int e = blockIdx.x; e < p.E; e += p.n_cta) {
+            const uint8_t *lw = p.wbase + (size_t)l * p.layer_stride;
+            bulk_prefetch_l2(lw + p.off_rg + (size_t)e * p.d * 4, (uint32_t)p.d * 4);
+            bulk_prefetch_l2(lw + p.off_rgwo + (size_t)e * dq * 4, (uint32_t)dq * 4);
+          }
       }
+      const float *const rgl = reinterpret_cast<const float *>(p.wbase + (size_t)l * p.layer_stride + p.off_rg);
+      RouterRow rrow;
+      if constexpr (MOE) rrow = moe_router_fetch(p, rgl, p.d);
       if (l > 0) ss = stage_f32(s, p.x, p.d, true);
       consume_region(s, p.nslot, rp, rq.r1 - rq.r0, p.d, 1.0f / sqrtf(ss / (float)p.d + p.eps), g);
       consumer_sync();
+      if constexpr (MOE) moe_router_part(p, s, rrow, rgl, p.d, p.rlog);  // rg x, on the staged x
       epilogue_qkv(p, s, l, pos, rq.r0, rq.r1);
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
       if (l == 0 && blockIdx.x == 0 && tid == 0) p.ctl->amax[(t + 1) & 1] = 0ull;  // every CTA has read it
@@ -634,22 +686,23 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
       // [WO] h = x + Wo o
+      const float *const rgwol = reinterpret_cast<const float *>(p.wbase + (size_t)l * p.layer_stride + p.off_rgwo);
+      if constexpr (MOE) rrow = moe_router_fetch(p, rgwol, dq);
       stage_f32(s, p.o, dq, false);
       consume_region(s, p.nslot, rp, ro.r1 - ro.r0, dq, 1.0f, g);
       consumer_sync();
+      if constexpr (MOE) moe_router_part(p, s, rrow, rgwol, dq, p.rlog + p.E);  // rgwo o, on the staged o
       for (int i = tid; i < ro.r1 - ro.r0; i += NCT) p.h[ro.r0 + i] = hs[i] = xs[i] + s.out[i];
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
       if constexpr (MOE) {
-        // [ROUTER] logits of u = inv_rms(h) * (g o h); the staged g o h stays for the experts, also split into
-        // fp16 high and low parts (after the fp32 copy) for their tensor-core GEMVs
+        // [SELECT] stage g o h for the experts, also split into fp16 high and low parts for their tensor-core
+        // GEMVs, and inv_rms(h); the router logits are then inv_rms(h) * (rg x + rgwo o), both already summed
         __half *const xgu = reinterpret_cast<__half *>(s.vec + p.d);
         ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d, xgu);
         const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
-        moe_router(p, s, l, inv);
-        if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
         const MoeSel sel = moe_sel(p, s);
-        moe_select(p, s, sel, t, l);
+        moe_select(p, s, sel, t, l, inv);
         // row scales of this CTA's rows of the routed experts, copied while the first tiles are in flight
         const int Re = rg.r1 - rg.r0, Rd = ro.r1 - ro.r0;
         float *const scg = s.out + p.out_moe + MOE_SEL_FLOATS, *const scd = scg + p.top_k * Re;

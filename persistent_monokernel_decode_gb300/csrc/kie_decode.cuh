@@ -61,16 +61,17 @@ struct DecodeParams {
   float *out_logits;   // [n][V] device or null
   unsigned long long timeout_ns;
   int skip_cta, skip_barrier;
-  // sparse-MoE FFN (E > 0; E == 0 is the dense FFN above). Per layer: a router [E][d] (fp16, row-major) and E
-  // SwiGLU experts of width F with FP8 E4M3 weights in the packed layout with FP8_TILE_COLS-wide blocks, each
-  // row with an fp32 scale. In the layer block: off_router; off_egu + e * egu_bytes = expert e's gate/up rows
-  // interleaved [2F][d]; off_edn + e * edn_bytes = its down rows [d][F]; off_esgu: scales [E][2F] (interleaved
-  // like the rows); off_esdn: scales [E][d].
+  // sparse-MoE FFN (E > 0; E == 0 is the dense FFN above). Per layer: the router folded by linearity, rg =
+  // router o g_ffn [E][d] and rgwo = rg Wo [E][dq] (fp32, row-major), and E SwiGLU experts of width F with FP8
+  // E4M3 weights in the packed layout with FP8_TILE_COLS-wide blocks, each row with an fp32 scale. In the layer
+  // block: off_rg, off_rgwo; off_egu + e * egu_bytes = expert e's gate/up rows interleaved [2F][d]; off_edn +
+  // e * edn_bytes = its down rows [d][F]; off_esgu: scales [E][2F] (interleaved like the rows); off_esdn: scales
+  // [E][d].
   int E, top_k;
   int out_moe;  // floats into the row-result area: the selection (MOE_SEL_FLOATS), then the staged row scales
-  long long off_router, off_egu, off_edn, off_esgu, off_esdn, egu_bytes, edn_bytes;
+  long long off_rg, off_rgwo, off_egu, off_edn, off_esgu, off_esdn, egu_bytes, edn_bytes;
   const float *gffn;  // [L][d] FFN RMSNorm gains (fp32), applied to the staged vector (FP8 weights keep them out)
-  float *rlog;        // [E] router logits of the current layer
+  float *rlog;        // [2][E] the current layer's partial router logits: rg x and rgwo o
   // testing aids (device, or null): forced_experts [n][L][top_k] replaces each layer's own top_k selection (the
   // routing weights are still the softmax of this launch's router logits over the given experts); out_experts
   // [n][L][top_k] receives the kernel's own selection, in selection order

@@ -80,7 +80,31 @@ __global__ void pack_fp8_kernel(const uint8_t *a, const uint8_t *b, uint8_t *dst
   }
 }
 
+// The sparse-MoE router folded through the WO projection: out[e][k] = sum_j rg[e][j] * wo[j][k] for an fp32
+// [E, d] matrix rg (the router with the FFN RMSNorm gain applied) and the fp16 [d, dq] matrix Wo, accumulated in
+// fp64 in index order and rounded to fp32. One thread per output; a warp's threads share e, so rg is a
+// broadcast and Wo is read in coalesced rows.
+__global__ void fold_router_kernel(const float *rg, const uint16_t *wo, float *out, int E, int d, int dq) {
+  const long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  if (idx >= (long long)E * dq) return;
+  const int e = (int)(idx / dq), k = (int)(idx % dq);
+  double acc = 0.0;
+  for (int j = 0; j < d; ++j) {
+    __half_raw r;
+    r.x = wo[(size_t)j * dq + k];
+    acc = fma((double)rg[(size_t)e * d + j], (double)__half2float(__half(r)), acc);
+  }
+  out[idx] = (float)acc;
+}
+
 }  // namespace kie
+
+cudaError_t kie_launch_fold_router(const float *rg, const uint16_t *wo, float *out, int E, int d, int dq,
+                                   cudaStream_t stream) {
+  const long long n = (long long)E * dq;
+  kie::fold_router_kernel<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(rg, wo, out, E, d, dq);
+  return cudaGetLastError();
+}
 
 cudaError_t kie_launch_pack_fp8(const uint8_t *a, const uint8_t *b, uint8_t *dst, int M, int K, int n_cta,
                                 cudaStream_t stream) {

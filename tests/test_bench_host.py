@@ -34,7 +34,8 @@ def test_phase_bytes_add_up_to_a_layer():
     assert (b["qkv"] + b["wo"] + b["gu"] + b["down"]) * TWO_B.n_layers == layer
     assert b["att"] == 2 * 2 * TWO_B.n_kv_heads * TWO_B.head_dim * 145
     assert bench.phase_names(TWO_B) == ["qkv", "att", "wo", "gu", "down"]
-    assert bench.phase_names(MOE_M) == ["qkv", "att", "wo", "router", "egu", "edown"]
+    # the router is folded into the QKV and WO phases: five grid phases per MoE layer
+    assert bench.phase_names(MOE_M) == ["qkv", "att", "wo", "egu", "edown"]
     m = bench.phase_bytes(MOE_M, 300)
     layer_moe = (MOE_M.weight_bytes_per_token() - m["lm"]) // MOE_M.n_layers
     assert m["qkv"] + m["wo"] + m["router"] + m["egu"] + m["edown"] == layer_moe

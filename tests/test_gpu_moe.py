@@ -189,7 +189,8 @@ def test_moe_tiny_split_calls_and_prefill_pieces_are_exact(tiny):
     parts = np.concatenate([dec.decode(7), dec.decode(1), dec.decode(12)])
     assert np.array_equal(whole, parts)
     st = dec.barrier_stats()
-    assert st["barriers"] == 12 * (6 * MOE_TINY.n_layers + 1)  # 6 grid phases per MoE layer, + the LM head
+    # 5 grid phases per MoE layer (the router is folded into the QKV and WO phases), + the LM head
+    assert st["barriers"] == 12 * (5 * MOE_TINY.n_layers + 1)
 
 
 def test_moe_joint_expert_permutation_leaves_the_logits_bit_identical(kie):
@@ -269,4 +270,4 @@ def test_moe_m_full_decode_properties(moe_m):
     dec.prefill(prompt)
     parts = np.concatenate([dec.decode(200), dec.decode(n - 200)])
     assert np.array_equal(whole, parts)
-    assert dec.barrier_stats()["barriers"] == (n - 200) * (6 * MOE_M.n_layers + 1)
+    assert dec.barrier_stats()["barriers"] == (n - 200) * (5 * MOE_M.n_layers + 1)
