@@ -232,8 +232,10 @@ int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
  * expert weights are OCP FP8 E4M3 ("fn": no infinities, max 448) codes, one fp32 scale per row, the weight
  * being code value * row scale. out = sum over the routed experts j of w_j * Wd_j (silu(Wg_j u) * (Wu_j u)).
  * Attention, norms, embedding and LM head are those of the dense model. Decode runs the same monokernel with
- * the router, the top_k selection and the two expert projections as grid phases: after the router the
- * producer streams only the routed experts' FP8 tiles.
+ * the router folded by linearity into the QKV and WO phases (its logits are inv_rms(h) * (R diag(g) x +
+ * R diag(g) Wo o), the two products precomputed in fp32 at creation), the top_k selection right after the WO
+ * barrier, and the two expert projections as grid phases: after the selection the producer streams only the
+ * routed experts' FP8 tiles.
  *
  * Requirements: 1 <= n_experts <= 256, 1 <= top_k <= min(8, n_experts), d_model and ffn_dim multiples of 16.
  * Prefill of a MoE ctx runs the prompt through the decode kernel one position after another (teacher forcing,
@@ -257,8 +259,9 @@ typedef struct {
 int kie_query_buffers_moe(const kie_config *cfg, const kie_moe_config *moe, int n_cta, kie_buffer_sizes *out);
 
 /* kie_create / kie_create_with_buffers for a sparse-MoE model: the expert matrices are packed per CTA in
- * 512-code column blocks (kie_packed_offset_fp8), gate and up rows interleaved; the router and the FFN gains
- * are stored as given (the gain multiplies the staged vector, not the FP8 weights). */
+ * 512-code column blocks (kie_packed_offset_fp8), gate and up rows interleaved; the router is stored folded
+ * (R diag(g) and R diag(g) Wo, fp32, the second product accumulated in fp64 on the device) and the FFN gains
+ * as given (the gain multiplies the staged vector, not the FP8 weights). */
 int kie_create_moe(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w, const kie_moe_weights *mw,
                    void *stream, kie_ctx **out);
 int kie_create_moe_with_buffers(const kie_config *cfg, const kie_moe_config *moe, const kie_weights *w,
