@@ -112,6 +112,12 @@ __device__ __forceinline__ int key_index(unsigned long long key) {
   return (int)(0xFFFFFFFFu - (unsigned)(key & 0xFFFFFFFFull));
 }
 
+// The float a key was made from (argmax_key's order-preserving map inverted, bit for bit).
+__device__ __forceinline__ float key_value(unsigned long long key) {
+  const unsigned ord = (unsigned)(key >> 32);
+  return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+}
+
 // ---- split-KV attention -----------------------------------------------------------------------------------
 
 // Piece `sp` of KV head `kh`: positions [j0, j1) of the c cached ones. Emits the unnormalised partial (m, l, o)
@@ -504,56 +510,70 @@ __device__ inline void moe_router_part(const DecodeParams &p, Smem &s, const Rou
   }
 }
 
-// Every CTA, after the WO barrier: the router logits inv * (rg x + rgwo o), the top_k largest (the lowest id
-// first among equal ones), in descending order, and the softmax over them; warp 0 computes it (all CTAs get
-// identical results from identical inputs), publishes it to the producer through the selection mbarrier, and every
-// consumer sees it after the closing consumer_sync. With p.forced_experts the given experts of (token t, layer l)
-// are used instead of the own selection (which still goes to p.out_experts).
-__device__ __forceinline__ float moe_logit(const DecodeParams &p, int e, float inv) {
-  return (__ldcg(p.rlog + e) + __ldcg(p.rlog + p.E + e)) * inv;
+// Warp 0 of every CTA, right after the WO barrier: the top_k experts, chosen on the unnormalised router sums
+// rg x + rgwo o (the logits are these times inv_rms(h), one positive factor for all experts, so the order is the
+// logits' order; only sums whose scaled values would round to the same float can rank differently, and such
+// ties either side may break), in descending order, the lowest id first among equal ones. All CTAs get identical
+// results from identical inputs. The ids go to the producer through the selection mbarrier at once, before the
+// staging of g o h, so the routed experts' first tiles are on their way while the CTA stages. With
+// p.forced_experts the given experts of (token t, layer l) are used instead of the own selection (which still
+// goes to p.out_experts). Returns in lane j < top_k the sum of the j-th selected expert.
+__device__ __forceinline__ float moe_sum(const DecodeParams &p, int e) {
+  return __ldcg(p.rlog + e) + __ldcg(p.rlog + p.E + e);
 }
 
-__device__ inline void moe_select(const DecodeParams &p, const Smem &s, const MoeSel &sel, int t, int l, float inv) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  if (tid < 32) {
-    constexpr int PER = MAX_EXPERTS / 32;
-    unsigned long long key[PER];
+__device__ inline float moe_select_ids(const DecodeParams &p, const MoeSel &sel, int t, int l) {
+  const int lane = threadIdx.x & 31;
+  constexpr int PER = MAX_EXPERTS / 32;
+  unsigned long long key[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      key[i] = e < p.E ? argmax_key(moe_logit(p, e, inv), e) : 0ull;
-    }
-    int mine = 0;
-    for (int j = 0; j < p.top_k; ++j) {
-      unsigned long long b = 0ull;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) b = key[i] > b ? key[i] : b;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
-        b = other > b ? other : b;
-      }
-      const int id = key_index(b);
-#pragma unroll
-      for (int i = 0; i < PER; ++i)
-        if (lane + 32 * i == id) key[i] = 0ull;
-      if (lane == j) mine = id;
-    }
-    const size_t at = ((size_t)t * p.L + l) * p.top_k + lane;
-    if (p.out_experts && blockIdx.x == 0 && lane < p.top_k) p.out_experts[at] = mine;
-    if (p.forced_experts && lane < p.top_k) mine = p.forced_experts[at];  // ids checked on the host
-    const float v = lane < p.top_k ? moe_logit(p, mine, inv) : -INFINITY;
-    const float mx = warp_max(v);
-    const float ev = lane < p.top_k ? expf(v - mx) : 0.f;
-    const float sum = warp_sum(ev);
-    if (lane < p.top_k) {
-      sel.ids[lane] = mine;
-      sel.wts[lane] = ev / sum;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(sel.bar);
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = e < p.E ? argmax_key(moe_sum(p, e), e) : 0ull;
   }
-  consumer_sync();
+  int mine = 0;
+  unsigned long long mkey = 0ull;  // lane j: the key of the j-th largest sum
+  for (int j = 0; j < p.top_k; ++j) {
+    unsigned long long b = 0ull;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) b = key[i] > b ? key[i] : b;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+      b = other > b ? other : b;
+    }
+    const int id = key_index(b);
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (lane + 32 * i == id) key[i] = 0ull;
+    if (lane == j) {
+      mine = id;
+      mkey = b;
+    }
+  }
+  const size_t at = ((size_t)t * p.L + l) * p.top_k + lane;
+  if (p.out_experts && blockIdx.x == 0 && lane < p.top_k) p.out_experts[at] = mine;
+  // the selected sums come back out of their keys (no second read); forced ids read theirs
+  float v = lane < p.top_k ? key_value(mkey) : 0.f;
+  if (p.forced_experts && lane < p.top_k) {
+    mine = p.forced_experts[at];  // ids checked on the host
+    v = moe_sum(p, mine);
+  }
+  if (lane < p.top_k) sel.ids[lane] = mine;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(sel.bar);
+  return v;
+}
+
+// Warp 0, once inv_rms(h) is known: the routing weights, the softmax over the selected logits v_j * inv (read by
+// the consumers after the expert gate/up phase).
+__device__ inline void moe_select_weights(const DecodeParams &p, const MoeSel &sel, float v, float inv) {
+  const int lane = threadIdx.x & 31;
+  const float x = lane < p.top_k ? v * inv : -INFINITY;
+  const float mx = warp_max(x);
+  const float ev = lane < p.top_k ? expf(x - mx) : 0.f;
+  const float sum = warp_sum(ev);
+  if (lane < p.top_k) sel.wts[lane] = ev / sum;
 }
 
 __device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard &g, bool moe) {
@@ -696,13 +716,16 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
       if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;
 
       if constexpr (MOE) {
-        // [SELECT] stage g o h for the experts, also split into fp16 high and low parts for their tensor-core
-        // GEMVs, and inv_rms(h); the router logits are then inv_rms(h) * (rg x + rgwo o), both already summed
+        // [SELECT] the routed experts from rg x + rgwo o (both already summed), published to the producer by warp
+        // 0 while the others stage g o h for the experts, also split into fp16 high and low parts for their
+        // tensor-core GEMVs, and inv_rms(h); then the routing weights from the logits inv_rms(h) * (rg x + rgwo o)
         __half *const xgu = reinterpret_cast<__half *>(s.vec + p.d);
-        ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d, xgu);
-        const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
         const MoeSel sel = moe_sel(p, s);
-        moe_select(p, s, sel, t, l, inv);
+        float vsel = 0.f;
+        if (tid < 32) vsel = moe_select_ids(p, sel, t, l);
+        ss = stage_f32_gain(s, p.h, p.gffn + (size_t)l * p.d, p.d, xgu);  // ends with consumer_sync: ids visible
+        const float inv = 1.0f / sqrtf(ss / (float)p.d + p.eps);
+        if (tid < 32) moe_select_weights(p, sel, vsel, inv);
         // row scales of this CTA's rows of the routed experts, copied while the first tiles are in flight
         const int Re = rg.r1 - rg.r0, Rd = ro.r1 - ro.r0;
         float *const scg = s.out + p.out_moe + MOE_SEL_FLOATS, *const scd = scg + p.top_k * Re;
