@@ -758,13 +758,20 @@ __device__ inline void consumer_main(const DecodeParams &p, Smem &s, const Guard
         __half *const xdn = reinterpret_cast<__half *>(s.vec);
         const int KA = p.top_k * p.F;
         stage_split(p.a, KA, xdn);
+        // one row group per expert (the usual case): each expert's partial sums stay in their own area of s.vec
+        // and all are added after one consumer_sync, when s.vec has room for the top_k areas after a
+        const bool dfr = Rd <= TILE_ROWS && p.vec_floats >= KA + p.top_k * FP8_RED_FLOATS;
         for (int j = 0; j < p.top_k; ++j)
           consume_region_fp8(s, p.nslot, rp, Rd, p.F, xdn + (size_t)j * p.F, xdn + KA + (size_t)j * p.F, 1.0f,
-                             s.out + j * Rd, s.vec + KA, g);
+                             s.out + j * Rd, s.vec + KA + (dfr ? j * FP8_RED_FLOATS : 0), g, dfr);
         consumer_sync();
+        const bool rag = p.F % FP8_TILE_COLS != 0;
         for (int i = tid; i < Rd; i += NCT) {
           float acc = 0.f;
-          for (int j = 0; j < p.top_k; ++j) acc += sel.wts[j] * (scd[j * Rd + i] * s.out[j * Rd + i]);
+          for (int j = 0; j < p.top_k; ++j) {
+            const float v = dfr ? fp8_group_sum(s.vec + KA + j * FP8_RED_FLOATS, i, Rd, rag) * 1.0f : s.out[j * Rd + i];
+            acc += sel.wts[j] * (scd[j * Rd + i] * v);
+          }
           p.x[ro.r0 + i] = xs[i] = hs[i] + acc;
         }
         if (!(ok = grid_barrier(p, s, gen, g, wait_ns))) break;

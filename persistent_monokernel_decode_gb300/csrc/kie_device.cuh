@@ -586,15 +586,30 @@ __device__ __forceinline__ void tile_loop_fp8_mma(const uint8_t *ring, uint64_t 
   }
 }
 
+// Row r (< rows) of an FP8 row group from the partial sums its warps left in `red`, in a fixed order: the
+// tensor-core warps that own the row (all of them for <= 16 rows, every other one otherwise), then the ragged
+// block's sum.
+__device__ __forceinline__ float fp8_group_sum(const float *red, int r, int rows, bool ragged) {
+  const int nmb = rows > 16 ? 2 : 1;
+  float v = 0.f;
+  for (int w = 0; w < NCW; ++w)
+    if (nmb == 1 || (w & 1) == (r >> 4)) v += red[w * TILE_ROWS + r];
+  if (ragged) v += red[NCW * TILE_ROWS + r];
+  return v;
+}
+
 // out[i] = scale * sum_k Q[r0 + i][k] * x[k] over the R rows of this CTA in one packed FP8 region (codes taken at
 // their E4M3 value; the caller applies the row scales). x is given as its fp16 high part xh and low part xl
 // (K values each). Full 512-code blocks run on the tensor cores (fp8_block_mma); a ragged last block takes the
 // CUDA-core path with x = xh + xl, one 16-code chunk per lane and row, rows warp, warp + NCW, ... Per row group
-// the partial sums meet in `red` (9 x TILE_ROWS floats) and are added in a fixed order. A thread whose wait
-// gives up raises the CTA abort flag and walks the same tile sequence, like consume_region.
+// the partial sums meet in `red` (9 x TILE_ROWS floats) and are added in a fixed order (fp8_group_sum). With
+// `defer` (R <= TILE_ROWS only) the region stops there: no consumer_sync, `out` untouched, the partial sums left
+// in `red` for the caller, who syncs once after several regions (each with its own `red`) and adds them itself.
+// A thread whose wait gives up raises the CTA abort flag and walks the same tile sequence, like consume_region.
 static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingPos &rp, int R, int K,
                                                        const __half *xh, const __half *xl, float scale,
-                                                       float *out, float *red, const Guard &g) {
+                                                       float *out, float *red, const Guard &g,
+                                                       bool defer = false) {
   bool ok = s.flags[0] == 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, fg = lane >> 2, ft = lane & 3;
   const uint8_t *const ring = s.ring;
@@ -655,14 +670,9 @@ static __device__ __noinline__ void consume_region_fp8(Smem &s, int nslot, RingP
         }
       }
     }
+    if (defer) break;  // R <= TILE_ROWS: this was the only row group
     consumer_sync();
-    for (int r = tid; r < rows; r += NCT) {
-      float v = 0.f;
-      for (int w = 0; w < NCW; ++w)
-        if (nmb == 1 || (w & 1) == (r >> 4)) v += red[w * TILE_ROWS + r];
-      if (ragged) v += red[NCW * TILE_ROWS + r];
-      out[g0 + r] = v * scale;
-    }
+    for (int r = tid; r < rows; r += NCT) out[g0 + r] = fp8_group_sum(red, r, rows, ragged) * scale;
     consumer_sync();  // red is reused by the next row group
   }
   rp.slot = slot;
