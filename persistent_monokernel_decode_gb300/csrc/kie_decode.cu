@@ -537,11 +537,13 @@ __device__ inline float moe_select_ids(const DecodeParams &p, const MoeSel &sel,
     unsigned long long b = 0ull;
 #pragma unroll
     for (int i = 0; i < PER; ++i) b = key[i] > b ? key[i] : b;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
-      b = other > b ? other : b;
-    }
+    // the warp's largest 64-bit key from two 32-bit reductions: the largest high half, then the largest low half
+    // among the lanes whose own largest key has that high half (a lane's largest key is its largest low half
+    // for its largest high half)
+    const unsigned bh = (unsigned)(b >> 32);
+    const unsigned mh = __reduce_max_sync(0xffffffffu, bh);
+    const unsigned ml = __reduce_max_sync(0xffffffffu, bh == mh ? (unsigned)b : 0u);
+    b = ((unsigned long long)mh << 32) | ml;
     const int id = key_index(b);
 #pragma unroll
     for (int i = 0; i < PER; ++i)
