@@ -610,6 +610,12 @@ __device__ inline void producer_main(const DecodeParams &p, Smem &s, const Guard
             ok = produce_region(gub + (size_t)sel.ids[j] * p.egu_bytes, Re, p.d, s, p.nslot, rp, policy, g, 1,
                                 FP8_TILE_COLS);
         }
+        // the down tiles only once the last gate/up tile has landed: issued with them, they share HBM with the
+        // gate/up burst that the phase waits for, while they are needed only after the next barrier
+        if (ok && Re > 0) {
+          const bool wrap = rp.slot == 0;
+          ok = wait_mbar(&s.full[wrap ? p.nslot - 1 : rp.slot - 1], wrap ? rp.phase ^ 1u : rp.phase, g);
+        }
         for (int j = 0; j < p.top_k && ok; ++j)
           ok = produce_region(lw + p.off_edn + (size_t)sel.ids[j] * p.edn_bytes + (size_t)ro.r0 * p.F, ro.r1 - ro.r0,
                               p.F, s, p.nslot, rp, policy, g, 1, FP8_TILE_COLS);
