@@ -130,8 +130,9 @@ int kie_decode_forced(kie_ctx *ctx, int n, const int32_t *forced, int32_t *out_t
  * As kie_decode_forced, plus: forced_experts (host int32 [n][n_layers][top_k], or NULL) replaces the selection
  * of every layer of every forward by the given expert ids (the routing weights stay the softmax of the GPU's
  * router logits over the given experts, in the given order); out_experts (host int32 [n][n_layers][top_k], or
- * NULL) receives the GPU's own selection (descending router logit, the lowest id first among equal ones),
- * computed whether or not it is overridden. It may also start a sequence (no prior prefill: the forwards then
+ * NULL) receives the GPU's own selection (descending router logit, the lowest id first among equal ones; ranked
+ * on the logits before their common positive RMS factor, so sums whose scaled values round to the same float may
+ * rank either way), computed whether or not it is overridden. It may also start a sequence (no prior prefill: the forwards then
  * ingest the forced tokens like a prompt, and out_tokens[0] is -1). Errors: INVALID (a dense model with
  * non-NULL expert arguments, an expert id outside [0, n_experts)), and those of kie_decode_forced. */
 int kie_decode_forced_routed(kie_ctx *ctx, int n, const int32_t *forced, const int32_t *forced_experts,
@@ -234,8 +235,10 @@ int kie_decode_noalloc(kie_ctx *ctx, int n, int32_t *out_tokens_dev);
  * Attention, norms, embedding and LM head are those of the dense model. Decode runs the same monokernel with
  * the router folded by linearity into the QKV and WO phases (its logits are inv_rms(h) * (R diag(g) x +
  * R diag(g) Wo o), the two products precomputed in fp32 at creation), the top_k selection right after the WO
- * barrier, and the two expert projections as grid phases: after the selection the producer streams only the
- * routed experts' FP8 tiles.
+ * barrier (ranked on the unnormalised sums, whose order the positive factor inv_rms(h) does not change, so the
+ * experts are known before h is staged; the routing weights follow once inv_rms(h) is), and the two expert
+ * projections as grid phases: after the selection the producer streams only the routed experts' FP8 tiles, the
+ * down projection's once the gate/up tiles have landed.
  *
  * Requirements: 1 <= n_experts <= 256, 1 <= top_k <= min(8, n_experts), d_model and ffn_dim multiples of 16.
  * Prefill of a MoE ctx runs the prompt through the decode kernel one position after another (teacher forcing,
