@@ -85,7 +85,7 @@ TWO_B = ModelConfig("llama2b", n_layers=25, d_model=2560, n_heads=20, n_kv_heads
 
 # the sparse-MoE model (FP8 experts) and a tiny one of the same structure
 MOE_M = MoEConfig("moe", n_layers=24, d_model=2048, n_heads=16, n_kv_heads=4, head_dim=128, ffn_dim=1024,
-                  vocab=32000, seed=2, n_experts=64, top_k=4, expert_ffn=1024)
+                  vocab=32000, seed=2, gain_std=0.01, n_experts=64, top_k=4, expert_ffn=1024)
 MOE_TINY = MoEConfig("moe_tiny", n_layers=2, d_model=256, n_heads=4, n_kv_heads=2, head_dim=64, ffn_dim=128,
                      vocab=4096, seed=3, gain_std=0.01, n_experts=8, top_k=4, expert_ffn=128)
 
